@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark: MLA paged decode throughput on GB300, in KV-tokens x heads per second.
+
+One step = one full decode call (plan as the workload needs it, attention over
+every request, split merge, and for the context-parallel workload the LSE merge
+of the shards) over one batch of synthetic input already resident in HBM.
+
+  python bench.py [--config draft_block_bf16] [--steps K] [--warmup W] [--gpus N]
+  python bench.py --impl reference ...     # the float64 CPU oracle on the host cores
+
+Under torchrun (N > 1) every rank decodes its own batch of the same shape (requests
+are independent: weak scaling, no collective on the data path); rank 0 prints the
+JSON line with the sum of units over ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_inputs as mi  # noqa: E402
+
+METRIC = "MLA decode: KV-tokens·heads/s, achieved HBM GB/s and % roofline on 1 GB300"
+FLOP_PER_PAIR = 2 * 576 + 2 * 512          # QK over 576 + PV over 512, per (query row, visible entry)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def build_workload(name: str):
+    """Returns (workload_for_call, extra) with extra describing plan mode, cap, merge."""
+    if name == "tiny_causal_bf16":
+        return mi.tiny_causal_bf16(), dict(mode=1, cap=0, shards=None)
+    if name == "draft_block_bf16":
+        return mi.draft_block_bf16(), dict(mode=0, cap=8192, shards=None)
+    if name == "verify_fp8":
+        w = mi.verify_fp8()
+        return w, dict(mode=0, cap=w.meta["kv_len_cap"], shards=None)
+    if name == "long_skewed_fp8":
+        return mi.long_skewed_fp8(), dict(mode=1, cap=0, shards=None)
+    if name == "cp_shards_bf16":
+        sw = mi.cp_shards_bf16()
+        return sw.shards, dict(mode=1, cap=0, shards=sw)
+    raise SystemExit(f"unknown config {name}")
+
+
+def visible_pairs(w) -> int:
+    """Sum over query rows (t, h) of the number of visible KV entries."""
+    tot = 0
+    for b in range(w.batch):
+        L = int(w.kv_indptr[b + 1] - w.kv_indptr[b])
+        T = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        if not w.causal:
+            tot += L * T
+            continue
+        base = int(w.pos_base_per_req[b]) if w.pos_base_per_req is not None else w.pos_base
+        Lg = int(w.g_kv_indptr[b + 1] - w.g_kv_indptr[b]) if w.g_kv_indptr is not None else L
+        for t in range(T):
+            lim = Lg - T + t - base
+            tot += 0 if lim < 0 else min(L, lim // w.pos_stride + 1)
+    return tot * w.num_heads
+
+
+def algorithmic_bytes(w) -> int:
+    elem = 2 if w.kv_dtype == "bf16" else 1
+    nnz = int(w.kv_indptr[-1] - w.kv_indptr[0])
+    rows = w.total_q * w.num_heads
+    return nnz * 576 * elem + 4 * nnz + rows * (576 * 2 + 512 * 2 + 4)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            out = dict(FALLBACK_PEAKS)
+            for k in out:
+                if isinstance(d.get(k), (int, float)):
+                    out[k] = float(d[k])
+            out["source"] = "measured"
+            return out
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(w, shards, budget_s: float = 12.0, max_requests=None):
+    """Time the float64 oracle on whole requests of the workload until the budget is used.
+    Returns (units, seconds, requests_done, threads)."""
+    from oracle import mla_oracle as mo
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count()])
+    except Exception:
+        threads = os.cpu_count()
+    src = shards.full if shards is not None else w
+    order = list(range(src.batch))
+    units = 0
+    t0 = time.perf_counter()
+    done = 0
+    for b in order:
+        if max_requests is not None and done >= max_requests:
+            break
+        if shards is not None:
+            # all shards of request b, then the LSE merge: the same work the GPU step does
+            sh = shards.shards
+            reqs = [r * src.batch + b for r in range(shards.num_shards)]
+            Os, Ls = mo.mla_decode_workload(sh, requests=reqs)
+            q0, q1 = int(src.qo_indptr[b]), int(src.qo_indptr[b + 1])
+            parts_o = np.stack([Os[sh.qo_indptr[r]:sh.qo_indptr[r + 1]].reshape(-1, 512) for r in reqs])
+            parts_l = np.stack([Ls[sh.qo_indptr[r]:sh.qo_indptr[r + 1]].reshape(-1) for r in reqs])
+            mo.merge_states(parts_o, parts_l)
+            sub = _single_request(src, b)
+        else:
+            mo.mla_decode_workload(w, requests=[b])
+            sub = _single_request(w, b)
+        units += visible_pairs(sub)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return units, time.perf_counter() - t0, done, threads
+
+
+def _single_request(w, b):
+    import dataclasses
+    k0, k1 = int(w.kv_indptr[b]), int(w.kv_indptr[b + 1])
+    q0, q1 = int(w.qo_indptr[b]), int(w.qo_indptr[b + 1])
+    return dataclasses.replace(
+        w, kv_indptr=np.array([0, k1 - k0], np.int32), kv_indices=w.kv_indices[k0:k1],
+        qo_indptr=np.array([0, q1 - q0], np.int32), q_bits=w.q_bits[q0:q1],
+        pos_base_per_req=None if w.pos_base_per_req is None else w.pos_base_per_req[b:b + 1],
+        g_kv_indptr=None if w.g_kv_indptr is None else np.array(
+            [0, int(w.g_kv_indptr[b + 1] - w.g_kv_indptr[b])], np.int32))
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="draft_block_bf16", choices=mi.CONFIG_NAMES)
+    ap.add_argument("--algo", default="tensor", choices=["tensor", "cuda_core"])
+    ap.add_argument("--workers", type=int, default=0, help="plan workers (0 = kernel default)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w, extra = build_workload(args.config)
+        per_step = []
+        units_step = []
+        cores = os.cpu_count()
+        budget = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+        for i in range(args.warmup + args.steps):
+            u, s, done, cores = oracle_sample(w, extra["shards"], budget_s=budget, max_requests=None)
+            if i >= args.warmup:
+                per_step.append(s)
+                units_step.append(u)
+        value = sum(units_step) / sum(per_step)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "KV-tokens*heads/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": 1e3 * sum(per_step) / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.config, "sample": "whole requests until the per-step time budget"},
+                "cpu_baseline": {"value": value, "unit": "KV-tokens*heads/s", "cores": cores,
+                                 "kind": "oracle", "sample": f"whole requests, ~{budget:.0f} s per step"},
+                "e2e": {"value": value, "unit": "KV-tokens*heads/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    import token_mla_paged_gb300 as m
+
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_index = torch.cuda.current_device()
+
+    w, extra = build_workload(args.config)
+    shards = extra["shards"]
+    algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
+    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+    workers = args.workers or (sms // 2 if algo == m.MLA_ALGO_TENSOR else sms)
+    maxq = int(w.q_lens().max())
+    runner = m.DecodeRunner(w.batch, w.num_heads, maxq, mode=extra["mode"], num_workers=workers,
+                            kv_len_cap=extra["cap"])
+    if extra["mode"] == m.MLA_PLAN_STATIC:
+        runner.set_host_plan(None, w.qo_indptr)
+    dev = mi.to_device(w)
+    out_fp32 = shards is not None
+    o = torch.empty(w.total_q, w.num_heads, 512, device="cuda",
+                    dtype=torch.float32 if out_fp32 else torch.bfloat16)
+    lse = torch.empty(w.total_q, w.num_heads, device="cuda", dtype=torch.float32)
+    if shards is not None:
+        R = shards.full.total_q * shards.full.num_heads
+        om = torch.empty(R, 512, dtype=torch.bfloat16, device="cuda")
+        lm = torch.empty(R, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        runner.forward(o=o, lse=lse, algo=algo, **dev)
+        if shards is not None:
+            m.mla_merge_states(o.view(shards.num_shards, R, 512), lse.view(shards.num_shards, R), om, lm)
+
+    launches_per_step = 1 + (1 if extra["mode"] == m.MLA_PLAN_DYNAMIC else 0) + (1 if shards else 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    units = visible_pairs(shards.full if shards else w)
+    flops = FLOP_PER_PAIR * units
+    nbytes = algorithmic_bytes(w)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, info = m.mla_get_device_error(runner.workspace)
+    assert code == 0, f"device error {code} ({info})"
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(args.steps):
+            flush.zero_()                        # L2 flush between timed steps (not timed)
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    times = [a.elapsed_time(b) for a, b in evs]
+    ms = sum(times) / len(times)
+    ms_t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    # End to end through the public API: host (pinned) q + index lists in, O + LSE out.
+    q_h = dev["q"].cpu().pin_memory()
+    idx_h = {k: dev[k].cpu().pin_memory() for k in ("kv_indptr", "kv_indices", "qo_indptr")}
+    out_final = (om, lm) if shards is not None else (o, lse)
+    o_h = torch.empty_like(out_final[0], device="cpu").pin_memory()
+    l_h = torch.empty_like(out_final[1], device="cpu").pin_memory()
+    h2d = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in idx_h.values())
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        dev["q"].copy_(q_h, non_blocking=True)
+        for k, t in idx_h.items():
+            dev[k].copy_(t, non_blocking=True)
+        step()
+        o_h.copy_(out_final[0], non_blocking=True)
+        l_h.copy_(out_final[1], non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    e2e_t = torch.tensor([e2e_ms], device="cuda")
+    if world > 1:
+        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
+    e2e_ms = float(e2e_t.item())
+
+    peaks = load_peaks()
+    achieved_tf = flops / (ms * 1e-3) / 1e12
+    achieved_gbs = nbytes / (ms * 1e-3) / 1e9
+    line = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            u, s, done, cores = oracle_sample(w, shards, budget_s=12.0)
+            cpu = {"value": u / s, "unit": "KV-tokens*heads/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{done} whole request(s) of the same workload, {s:.1f} s"}
+        line = {
+            "metric": METRIC, "value": world * units / (ms_max * 1e-3), "unit": "KV-tokens*heads/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-kv/bf16-mma",
+            "data": "synthetic",
+            "config": {"workload": args.config, "batch": w.batch, "heads": w.num_heads,
+                       "q_len": int(w.q_lens().max()), "kv_tokens": int(w.kv_indptr[-1]),
+                       "kv_dtype": w.kv_dtype, "causal": w.causal, "plan": "static" if extra["mode"] == 0 else "dynamic",
+                       "algo": args.algo, "workers": workers, "l2": "flushed (256 MB write) between timed steps"},
+            "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"], "traffic": None,
+                         "peak_source": peaks["source"], "hbm_achieved_gbs": achieved_gbs,
+                         "hbm_frac": achieved_gbs / peaks["hbm_gbs"], "alg_flops": flops,
+                         "alg_bytes": nbytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": "KV-tokens*heads/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

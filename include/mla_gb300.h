@@ -1,0 +1,208 @@
+/*
+ * mla_gb300.h -- C ABI of the GB300 (sm_103a) MLA paged-decode library.
+ *
+ * Operation.  Multi-head latent attention decode in absorbed form over a
+ * page-size-1 latent KV cache, for a block of T query tokens per request:
+ *   - every KV entry is one 576-wide latent row (512 latent + 64 RoPE) shared
+ *     by all heads; scores use all 576 columns, the output lives in the first
+ *     512 ("[ROCm] Dspark MLA module", Details: absorb BMM, MLAAttention,
+ *     concat_and_cache_mla);
+ *   - each request's entries are a flat index list kv_indices[kv_indptr[b] ..
+ *     kv_indptr[b+1]) into the pool ("[ROCm][Spec Decode] Add Aiter MLA decode
+ *     support non-causal draft block", Purpose);
+ *   - the block is either non-causal (every token sees all committed entries,
+ *     same page, Purpose) or causal on global positions, including a
+ *     round-robin context-parallel shard whose global lengths come from
+ *     g_kv_indptr, and the call returns the log-sum-exp ("Speculative decode +
+ *     DCP on gfx1250", Problem);
+ *   - the pool is bf16 or fp8 e4m3fn with one per-tensor scale ("[ROCm][Spec
+ *     Decode] ...", section "Three pieces");
+ *   - long rows are split over the KV and merged through the LSE inside the
+ *     call, driven by a split plan that is deterministic in its inputs so a
+ *     CUDA-graph replay agrees with its capture; the plan is either built on
+ *     the host once from capacities (STATIC) or rebuilt on the device from the
+ *     real lengths at every call (DYNAMIC) ("[DSV4] Tuned ASM FP8 decode with
+ *     split plans; HCA on aiter's persistent V4-NM kernel", Summary parts 1
+ *     and 2).
+ *
+ * Definition, for request b, token t in [0,T_b), head h:
+ *   k_i = dec(pool[kv_indices[kv_indptr[b]+i]]) * kappa   (kappa = kv_scale for fp8, else 1)
+ *   s_i = softmax_scale * <q[t,h,0:576], k_i[0:576]>
+ *   visible(i) = !causal || base_b + i*pos_stride <= Lg_b - T_b + t
+ *   LSE[t,h] = ln sum_{visible} exp(s_i)      O[t,h,:] = sum exp(s_i - LSE) k_i[0:512]
+ *   no visible entry: O = 0, LSE = -inf.
+ * base_b = pos_base_per_req[b] if given, else pos_base; Lg_b = g_kv_indptr[b+1] -
+ * g_kv_indptr[b] if given, else the local length L_b.
+ *
+ * Layouts (row-major, contiguous):
+ *   q        bf16 [total_q, H, 576]        total_q = qo_indptr[B]
+ *   kv_pool  bf16 | fp8 [num_slots, 576]
+ *   o        bf16 | fp32 [total_q, H, 512]
+ *   lse      fp32 [total_q, H]  (natural log)
+ *   kv_indptr, qo_indptr int32 [B+1] (non-decreasing), kv_indices int32 [kv_indptr[B]]
+ *   Within request b, query row r = t*H + h; rows of one request are contiguous.
+ *
+ * Conventions.
+ *   - The caller owns every buffer.  The library never allocates device memory,
+ *     never synchronises and never reads device memory on the host inside
+ *     mla_decode_fwd / mla_decode_plan_device / mla_merge_states, so all three
+ *     can be captured in a CUDA graph.  `stream` is a cudaStream_t (NULL = the
+ *     legacy default stream).
+ *   - Every function returns an mla_status and never aborts the process.  Bad
+ *     host-visible arguments return MLA_ERR_INVALID_ARG / UNSUPPORTED / ... before
+ *     anything is enqueued.  Faults only the device can see (an index outside
+ *     [0, num_slots), a decreasing kv_indptr, a plan that does not match the
+ *     call, a bounded wait that ran out) are recorded in an error word inside
+ *     the workspace; the offending entries are treated as masked.  Read it with
+ *     mla_get_device_error.
+ *   - Device pointers must be 16-byte aligned (q, kv_pool, o) and 4-byte
+ *     aligned (index arrays, lse).
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_ABI_VERSION 1
+#define MLA_D_QK 576             /* latent 512 + RoPE 64 */
+#define MLA_D_V 512
+#define MLA_ROWS_PER_GROUP 128   /* query rows (t,h) handled together */
+#define MLA_BLOCK_N 64           /* KV entries per tile */
+#define MLA_MAX_SPLITS 16
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,
+  MLA_ERR_UNSUPPORTED = 2,
+  MLA_ERR_WORKSPACE_TOO_SMALL = 3,
+  MLA_ERR_PLAN_MISMATCH = 4,
+  MLA_ERR_CUDA = 5,
+  MLA_ERR_DEVICE_FAULT = 6
+} mla_status;
+
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
+typedef enum { MLA_OUT_BF16 = 0, MLA_OUT_FP32 = 1 } mla_out_dtype;
+typedef enum { MLA_PLAN_STATIC = 0, MLA_PLAN_DYNAMIC = 1 } mla_plan_mode;
+
+/* Kernel family.  MLA_ALGO_TENSOR (default) is the tcgen05/TMEM kernel;
+ * MLA_ALGO_CUDA_CORE is a plain CUDA-core kernel of the same operation, kept for
+ * cross-checks.  Both read the same plan and workspace. */
+typedef enum { MLA_ALGO_TENSOR = 0, MLA_ALGO_CUDA_CORE = 1 } mla_algo;
+
+/* Device error codes stored in the workspace error word. */
+typedef enum {
+  MLA_DEV_OK = 0,
+  MLA_DEV_BAD_INDEX = 1,        /* kv_indices[j] outside [0, num_slots); info = j        */
+  MLA_DEV_BAD_INDPTR = 2,       /* kv_indptr or qo_indptr decreasing; info = b            */
+  MLA_DEV_PLAN_MISMATCH = 3,    /* device plan header differs from the call's params     */
+  MLA_DEV_ROWS_MISMATCH = 4,    /* q length of request b differs from the plan; info = b */
+  MLA_DEV_WAIT_TIMEOUT = 5,     /* a bounded barrier wait ran out; info = site           */
+  MLA_DEV_PLAN_OVERFLOW = 6     /* device planner: items exceed the plan capacity        */
+} mla_device_error;
+
+/* Plan parameters.  The same struct is passed to the planner and to the forward
+ * call; both check the plan against it ("builder and impl call the same
+ * predicate").
+ *   batch        B >= 0 requests
+ *   num_heads    H >= 1
+ *   max_q_len    upper bound on T_b (sizes the plan and workspace)
+ *   num_workers  W >= 1: the plan aims at about W equal work items' worth of
+ *                splitting (use the number of persistent workers)
+ *   kv_len_cap   STATIC only: the KV length every request is planned for
+ *   mode         mla_plan_mode */
+typedef struct {
+  int32_t batch;
+  int32_t num_heads;
+  int32_t max_q_len;
+  int32_t num_workers;
+  int64_t kv_len_cap;
+  int32_t mode;
+  int32_t reserved;
+} mla_plan_params;
+
+/* Arguments of one forward call.  All pointers are device pointers except
+ * `params`, which points to host memory. */
+typedef struct {
+  const void* q;                     /* bf16 [total_q, H, 576] */
+  const void* kv_pool;               /* bf16 | fp8 [num_slots, 576] */
+  int64_t num_slots;
+  int32_t kv_dtype;                  /* mla_kv_dtype */
+  int32_t out_dtype;                 /* mla_out_dtype of o */
+  const int32_t* kv_indptr;          /* [B+1] */
+  const int32_t* kv_indices;         /* [kv_indptr[B]] */
+  const int32_t* qo_indptr;          /* [B+1] */
+  int32_t causal;                    /* 0 | 1 */
+  int32_t pos_base;                  /* global position of local entry 0 (default 0) */
+  int32_t pos_stride;                /* global position step per local entry (>= 1) */
+  int32_t algo;                      /* mla_algo */
+  const int32_t* pos_base_per_req;   /* nullable [B]: overrides pos_base per request */
+  const int32_t* g_kv_indptr;        /* nullable [B+1]: global lengths Lg_b */
+  float softmax_scale;               /* finite, > 0 */
+  float kv_scale;                    /* fp8: finite, > 0; ignored for bf16 */
+  void* o;                           /* [total_q, H, 512] */
+  float* lse;                        /* [total_q, H] */
+  const mla_plan_params* params;     /* host pointer */
+  void* plan_d;                      /* device plan buffer (STATIC: uploaded host plan;
+                                        DYNAMIC: rewritten by this call) */
+  size_t plan_bytes;
+  void* workspace_d;                 /* device workspace, >= the size mla_decode_plan_size gives */
+  size_t ws_bytes;
+} mla_fwd_args;
+
+/* ABI version (MLA_ABI_VERSION); lets a caller probe capabilities by number
+ * rather than by inspecting signatures. */
+int mla_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+const char* mla_status_string(int status);
+
+/* Sizes of the plan buffer and of the device workspace for these params.  Both
+ * are upper bounds valid for any lengths the params allow.  Host only. */
+mla_status mla_decode_plan_size(const mla_plan_params* params, size_t* plan_bytes,
+                                size_t* workspace_bytes);
+
+/* Build the plan on the host from host copies of kv_indptr / qo_indptr (each
+ * [B+1]; kv_indptr may be NULL in STATIC mode) into plan_h (plan_bytes, host
+ * memory).  Pure function of its inputs: the same inputs give the same bytes.
+ * Host only; no CUDA call. */
+mla_status mla_decode_plan(const mla_plan_params* params, const int32_t* kv_indptr_h,
+                           const int32_t* qo_indptr_h, void* plan_h, size_t plan_bytes);
+
+/* The same plan, computed by a kernel from device kv_indptr / qo_indptr and
+ * written to plan_d; enqueued on `stream`.  Bit-identical to mla_decode_plan on
+ * the same lengths.  Faults go to the workspace error word.  Requires
+ * B <= 4096 and an item capacity <= 8192. */
+mla_status mla_decode_plan_device(const mla_plan_params* params, const int32_t* kv_indptr_d,
+                                  const int32_t* qo_indptr_d, void* plan_d, size_t plan_bytes,
+                                  void* workspace_d, size_t ws_bytes, void* stream);
+
+/* Forward call: O and LSE for every (token, head) of the batch.  DYNAMIC mode
+ * first re-plans on the device from the real lengths.  Enqueued on `stream`. */
+mla_status mla_decode_fwd(const mla_fwd_args* args, void* stream);
+
+/* N-way merge of partial states over disjoint KV subsets:
+ *   o_parts [n, rows, dv] (fp32 | bf16, each normalised over its own subset),
+ *   lse_parts fp32 [n, rows]  ->  o [rows, dv] (o_dtype), lse fp32 [rows]:
+ *   M = max lse_s;  LSE = M + ln sum exp(lse_s - M);  O = sum exp(lse_s - LSE) O_s.
+ * States with lse = -inf add nothing; all -inf gives O = 0, LSE = -inf.  This is
+ * the combine step of round-robin context parallelism ("Speculative decode +
+ * DCP on gfx1250", Problem).  Enqueued on `stream`. */
+mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const float* lse_parts,
+                            int32_t n, int64_t rows, int32_t dv, void* o, int32_t o_dtype,
+                            float* lse, void* stream);
+
+/* Read and clear the workspace error word.  Synchronises `stream`; not for use
+ * while the stream is being captured.  *code receives an mla_device_error and
+ * *info its detail; returns MLA_ERR_DEVICE_FAULT when *code != 0. */
+mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -280,3 +280,27 @@ def flatten_block(w: Workload) -> Workload:
 
 
 CONFIG_NAMES = ["tiny_causal_bf16", "draft_block_bf16", "verify_fp8", "long_skewed_fp8", "cp_shards_bf16"]
+
+
+# ----------------------------------------------------------------------------
+# device upload (plain copies of the same bytes)
+# ----------------------------------------------------------------------------
+
+def to_device(w: Workload, device="cuda") -> dict:
+    """Copy a workload's bytes to the device as the tensors the C ABI takes."""
+    import torch
+    dev = torch.device(device)
+
+    def i32(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    q = torch.from_numpy(w.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    if w.kv_dtype == "bf16":
+        kv = torch.from_numpy(w.kv_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    else:
+        kv = torch.from_numpy(w.kv_bits).to(dev).view(torch.float8_e4m3fn)
+    return dict(q=q, kv_pool=kv, kv_dtype=0 if w.kv_dtype == "bf16" else 1,
+                kv_indptr=i32(w.kv_indptr), kv_indices=i32(w.kv_indices), qo_indptr=i32(w.qo_indptr),
+                causal=w.causal, softmax_scale=w.softmax_scale, kv_scale=w.kv_scale,
+                pos_base=w.pos_base, pos_stride=w.pos_stride,
+                pos_base_per_req=i32(w.pos_base_per_req), g_kv_indptr=i32(w.g_kv_indptr))

@@ -1,0 +1,139 @@
+"""CPU checks of the C ABI: the library loads, exports every declared symbol, and
+its host planner reproduces the plan specification bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import token_mla_paged_gb300 as m
+from oracle import plan_oracle as po
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "mla_gb300.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = m.library()
+    decl = _declared()
+    assert set(decl) == set(m.ABI_SYMBOLS)
+    for name in decl:
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings():
+    hdr = open(os.path.join(ROOT, "include", "mla_gb300.h")).read()
+    assert m.mla_abi_version() == int(re.search(r"#define MLA_ABI_VERSION (\d+)", hdr).group(1))
+    for s in range(7):
+        assert m.mla_status_string(s) and m.mla_status_string(s) != "unknown status"
+    assert m.mla_status_string(99) == "unknown status"
+
+
+def _host_vs_oracle(B, H, maxT, W, cap, mode, kvp, qop):
+    params = m.plan_params(B, H, maxT, W, cap, mode)
+    ours = m.mla_decode_plan(params, None if mode == po.STATIC else kvp, qop)
+    ref = po.build_plan(B, H, maxT, W, cap, mode, kvp, qop)
+    assert ours.shape == ref.shape
+    assert np.array_equal(ours, ref)
+
+
+def test_host_plan_matches_spec_worked_examples():
+    import json
+    cases = json.load(open(os.path.join(ROOT, "tests", "golden", "plan_worked_examples.json")))["cases"]
+    for c in cases:
+        kvp = None if c["kv_indptr"] is None else np.array(c["kv_indptr"], dtype=np.int32)
+        _host_vs_oracle(c["batch"], c["num_heads"], c["max_q_len"], c["num_workers"], c["kv_len_cap"],
+                        c["mode"], kvp, np.array(c["qo_indptr"], dtype=np.int32))
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_host_plan_matches_spec_random(seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(0, 70))
+    H = int(rng.choice([1, 3, 16, 64, 96, 128]))
+    maxT = int(rng.integers(0, 9))
+    W = int(rng.integers(1, 400))
+    mode = int(rng.integers(0, 2))
+    T = rng.integers(0, maxT + 1, size=B)
+    L = np.floor(np.exp(rng.uniform(0, np.log(300000), size=B))).astype(np.int64)
+    L[rng.random(B) < 0.15] = 0
+    kvp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    qop = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
+    cap = int(rng.integers(0, 200000))
+    _host_vs_oracle(B, H, maxT, W, cap, mode, kvp, qop)
+
+
+def test_host_plan_for_the_five_workloads():
+    import mla_inputs as mi
+    shapes = [(2, 16, 2, [37, 100], [2, 2]), (8, 64, 8, [8192] * 8, [8] * 8)]
+    rng = np.random.default_rng(7)
+    shapes.append((32, 128, 8, list(rng.integers(1024, 16385, 32)), [8] * 32))
+    shapes.append((64, 128, 4, list(np.floor(np.exp(rng.uniform(np.log(256), np.log(131072), 64))).astype(int)),
+                   list(rng.choice([1, 2, 4], 64))))
+    shapes.append((128, 96, 8, [4096] * 128, [8] * 128))
+    for B, H, maxT, L, T in shapes:
+        for W in (1, 76, 152, 608):
+            for mode in (po.STATIC, po.DYNAMIC):
+                kvp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+                qop = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
+                _host_vs_oracle(B, H, maxT, W, 16384, mode, kvp, qop)
+    assert mi.D_QK == 576
+
+
+def test_plan_sizes_follow_the_bounds():
+    p = m.plan_params(64, 128, 4, 76, 0, m.MLA_PLAN_DYNAMIC)
+    plan_bytes, ws_bytes = m.mla_decode_plan_size(p)
+    cap = 76 + 64 * 4
+    assert plan_bytes == 4 * (16 + 64 + 65 + 64 + 4 * cap)
+    assert ws_bytes >= 4 * cap * 128 * 512 + 4 * cap * 128 + 4 * 64 * 4 + 256
+
+
+def test_host_plan_rejects_bad_input():
+    with pytest.raises(m.MlaError):
+        m.mla_decode_plan(m.plan_params(2, 16, 2, 4, 0, m.MLA_PLAN_DYNAMIC),
+                          np.array([0, 5, 3]), np.array([0, 1, 2]))
+    with pytest.raises(m.MlaError):
+        m.mla_decode_plan(m.plan_params(2, 16, 1, 4, 0, m.MLA_PLAN_DYNAMIC),
+                          np.array([0, 5, 9]), np.array([0, 2, 3]))
+    with pytest.raises(m.MlaError):
+        m.mla_decode_plan(m.plan_params(2, 0, 1, 4, 0, m.MLA_PLAN_DYNAMIC),
+                          np.array([0, 5, 9]), np.array([0, 1, 2]))
+    with pytest.raises(m.MlaError):
+        m.mla_decode_plan_size(m.plan_params(1, 16, 1, 0, 0, m.MLA_PLAN_DYNAMIC))
+
+
+def test_fwd_rejects_bad_arguments_before_touching_the_device():
+    """Invalid host-visible arguments come back as a status; nothing is enqueued."""
+    import ctypes
+    lib = m.library()
+    params = m.plan_params(1, 16, 1, 4, 0, m.MLA_PLAN_DYNAMIC)
+    a = m.FwdArgs()
+    a.params = ctypes.pointer(params)
+    a.kv_dtype = 7
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1
+    a.kv_dtype = 0
+    a.softmax_scale = float("nan")
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1
+    a.softmax_scale = 0.07
+    a.pos_stride = 0
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1
+    a.pos_stride = 1
+    a.num_slots = 10
+    a.q = a.kv_pool = a.kv_indptr = a.kv_indices = a.qo_indptr = a.o = a.lse = 16
+    a.plan_d = 256
+    a.workspace_d = 256
+    a.plan_bytes = 4
+    a.ws_bytes = 1 << 30
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 3      # plan buffer too small
+    a.plan_bytes = 1 << 20
+    a.ws_bytes = 16
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 3      # workspace too small
+    a.ws_bytes = 1 << 30
+    a.q = 18
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1      # misaligned q
+    assert lib.mla_merge_states(None, 0, None, 0, 1, 512, None, 0, None, None) == 1

@@ -1,0 +1,90 @@
+// N-way merge of partial attention states (O_s, LSE_s) over disjoint KV
+// subsets, e.g. the per-shard results of round-robin context parallelism
+// ("Speculative decode + DCP on gfx1250", Problem: a verify pass over a
+// round-robin DCP shard with an LSE output).
+//
+//   M = max_s LSE_s;  LSE = M + ln sum_s exp(LSE_s - M);  O = sum_s exp(LSE_s - LSE) O_s
+//
+// One warp per row; lanes stride over the row's dv columns (coalesced), and the
+// per-state weights are computed once per row and broadcast with shuffles.
+// The work is HBM-bound: n*dv reads and dv writes per row.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace mla {
+namespace {
+
+__global__ void __launch_bounds__(256)
+mla_merge_states_kernel(const void* __restrict__ o_parts, int parts_fp32,
+                        const float* __restrict__ lse_parts, int n, int64_t rows, int dv,
+                        void* __restrict__ o, int o_fp32, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows;
+       r += warps_total) {
+    float M = -INFINITY;
+    for (int s = lane; s < n; s += 32) M = fmaxf(M, lse_parts[(int64_t)s * rows + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float tot = 0.f;
+    if (M != -INFINITY) {
+      for (int s = lane; s < n; s += 32) {
+        const float ls = lse_parts[(int64_t)s * rows + r];
+        if (ls != -INFINITY) tot += exp2f((ls - M) * 1.4426950408889634f);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    }
+    const float inv_tot = M != -INFINITY ? 1.f / tot : 0.f;
+    for (int d0 = 0; d0 < dv; d0 += 32) {
+      const int d = d0 + lane;
+      float acc = 0.f;
+      if (M != -INFINITY) {
+        for (int c = 0; c < n; c += 32) {
+          float w = 0.f;
+          if (c + lane < n) {
+            const float ls = lse_parts[(int64_t)(c + lane) * rows + r];
+            w = ls == -INFINITY ? 0.f : exp2f((ls - M) * 1.4426950408889634f) * inv_tot;
+          }
+          const int cnt = min(32, n - c);
+          for (int k = 0; k < cnt; ++k) {
+            const float wk = __shfl_sync(0xffffffffu, w, k);
+            if (d < dv && wk != 0.f) {
+              const int64_t off = ((int64_t)(c + k) * rows + r) * dv + d;
+              const float v = parts_fp32 ? static_cast<const float*>(o_parts)[off]
+                                         : bf16_bits_to_float(static_cast<const uint16_t*>(o_parts)[off]);
+              acc += wk * v;
+            }
+          }
+        }
+      }
+      if (d < dv) {
+        if (o_fp32) static_cast<float*>(o)[r * dv + d] = acc;
+        else static_cast<__nv_bfloat16*>(o)[r * dv + d] = __float2bfloat16_rn(acc);
+      }
+    }
+    if (lane == 0) lse[r] = M == -INFINITY ? -INFINITY : M + logf(tot);
+  }
+}
+
+}  // namespace
+
+mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const float* lse_parts,
+                               int n, int64_t rows, int dv, void* o, int o_fp32, float* lse,
+                               void* stream) {
+  static int num_sms = 0;
+  if (num_sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  const int64_t want = (rows + 7) / 8;
+  const int grid = (int)(want < (int64_t)num_sms * 16 ? want : (int64_t)num_sms * 16);
+  mla_merge_states_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(
+      o_parts, o_parts_fp32, lse_parts, n, rows, dv, o, o_fp32, lse);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace mla

@@ -1,0 +1,55 @@
+"""Buffer plumbing around the C ABI: allocates the plan and workspace with torch
+and issues the calls.  No attention arithmetic happens here."""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+
+from . import (MLA_ALGO_TENSOR, MLA_PLAN_DYNAMIC, MLA_PLAN_STATIC, mla_decode_fwd,
+               mla_decode_plan, mla_decode_plan_size, plan_params)
+
+
+def default_workers(device=None) -> int:
+    import torch
+    return int(torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count)
+
+
+class DecodeRunner:
+    """Owns one plan buffer and one workspace sized for `params`.
+
+    STATIC mode: call ``set_host_plan`` once (outside any graph) with host copies
+    of kv_indptr / qo_indptr; the plan is uploaded and then only read.
+    DYNAMIC mode: every ``forward`` re-plans on the device.
+    """
+
+    def __init__(self, batch: int, num_heads: int, max_q_len: int, *, mode: int = MLA_PLAN_DYNAMIC,
+                 num_workers: Optional[int] = None, kv_len_cap: int = 0, device="cuda"):
+        import torch
+        self.device = torch.device(device)
+        if num_workers is None:
+            num_workers = default_workers(self.device)
+        self.params = plan_params(batch, num_heads, max_q_len, num_workers, kv_len_cap, mode)
+        plan_bytes, ws_bytes = mla_decode_plan_size(self.params)
+        self.plan_d = torch.zeros(plan_bytes // 4, dtype=torch.int32, device=self.device)
+        self.workspace = torch.zeros((ws_bytes + 3) // 4, dtype=torch.int32, device=self.device)
+        self.host_plan: Optional[np.ndarray] = None
+
+    def set_host_plan(self, kv_indptr_h: Optional[np.ndarray], qo_indptr_h: np.ndarray) -> np.ndarray:
+        import torch
+        assert self.params.mode == MLA_PLAN_STATIC
+        plan = mla_decode_plan(self.params, kv_indptr_h, qo_indptr_h)
+        self.plan_d.copy_(torch.from_numpy(plan))
+        self.host_plan = plan
+        return plan
+
+    def forward(self, *, q, kv_pool, kv_dtype: int, kv_indptr, kv_indices, qo_indptr, causal: bool,
+                softmax_scale: float, kv_scale: float, o, lse, pos_base: int = 0,
+                pos_stride: int = 1, pos_base_per_req=None, g_kv_indptr=None,
+                algo: int = MLA_ALGO_TENSOR, stream=None) -> None:
+        mla_decode_fwd(q=q, kv_pool=kv_pool, kv_dtype=kv_dtype, kv_indptr=kv_indptr,
+                       kv_indices=kv_indices, qo_indptr=qo_indptr, causal=causal,
+                       softmax_scale=softmax_scale, kv_scale=kv_scale, o=o, lse=lse,
+                       params=self.params, plan_d=self.plan_d, workspace_d=self.workspace,
+                       pos_base=pos_base, pos_stride=pos_stride, pos_base_per_req=pos_base_per_req,
+                       g_kv_indptr=g_kv_indptr, algo=algo, stream=stream)
