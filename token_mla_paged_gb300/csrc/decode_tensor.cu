@@ -1,12 +1,743 @@
-// Tensor-core (tcgen05 / TMEM) MLA decode kernel for sm_103a.
+// Tensor-core MLA decode kernel for sm_103a (tcgen05 + TMEM + TMA gathers).
+//
+// All H*T query rows of a request share one stream of latent KV rows, so QK^T
+// over 576 columns and PV over 512 are dense contractions with M = 128 query
+// rows.  The fp32 accumulator of O[128, 512] alone fills the 512 TMEM columns of
+// an SM, so each work item runs on a cluster of two CTAs with different jobs:
+//
+//   rank 0, the score CTA: holds the item's Q[128, 576] in TMEM as the MMA's A
+//     operand, gathers K tiles [64 entries, 576] with TMA, computes
+//     S = Q K^T into a double-buffered TMEM tile, runs the masked online
+//     softmax (one thread per query row) and ships P (bf16) plus the per-row
+//     rescale factors and running max/sum into the peer's shared memory with a
+//     bulk copy.
+//   rank 1, the output CTA: gathers V tiles [64 entries, 512], accumulates
+//     O += P V in TMEM, rescales O when the score CTA raised its reference max,
+//     and writes O / l and the log-sum-exp (or the split partial and the fused
+//     split merge).
+//
+// The KV tile in shared memory is stored as 64-column chunks in the 128-byte
+// swizzled layout, so the same bytes serve as the K-major B operand of QK^T and
+// as the MN-major B operand of PV.  fp8 e4m3 pools are gathered as bytes and
+// converted to bf16 in registers by dedicated warps (exact: e4m3 -> f16 by the
+// hardware conversion, then the f16 bits are placed in a bf16 word, which
+// scales every value by 2^-112; the factor is folded into the logit and output
+// scales).
+//
+// Sources: absorbed-latent MLA decode with one 576-wide latent row per KV entry
+// ("[ROCm] Dspark MLA module", Details); page-size-1 index lists and the
+// non-causal draft block ("[ROCm][Spec Decode] Add Aiter MLA decode support
+// non-causal draft block", Purpose); causal mask on global positions over a
+// round-robin shard with an LSE output ("Speculative decode + DCP on gfx1250",
+// Problem); splits over the KV merged in-kernel ("[DSV4] Tuned ASM FP8 decode
+// with split plans; HCA on aiter's persistent V4-NM kernel", Summary part 2).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
+#include "tc_primitives.cuh"
 
 namespace mla {
+namespace {
 
-int tensor_kernel_available() { return 0; }
+using namespace tc;
 
-mla_status launch_decode_tensor(const DecodeParams&, void*) { return MLA_ERR_UNSUPPORTED; }
+constexpr int kThreads = 320;          // 10 warps
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpRow0 = 2;           // 4 row warps: softmax (rank 0) / correction+epilogue (rank 1)
+constexpr int kWarpConv0 = 6;          // 4 fp8 conversion warps
+constexpr int kStages = 2;             // KV tile ring
+constexpr int kPBufs = 2;              // P hand-off ring
+
+constexpr int kChunkBytes = kBlockN * 128;          // 64 entries x 64 bf16 columns = 8 KB
+constexpr int kKTileBytes = 9 * kChunkBytes;        // 576 columns (score CTA)
+constexpr int kVTileBytes = 8 * kChunkBytes;        // 512 columns (output CTA)
+constexpr int kF8Bytes = kBlockN * kDqk;            // fp8 staging, 64 x 576 bytes
+constexpr int kPBytes = kRows * 128;                // P: 128 rows x 64 bf16
+constexpr int kPStatsOff = kPBytes;                 // alpha[128], m[128], l[128], flags[4]
+constexpr int kPBufBytes = kPBytes + 3 * 512 + 512; // 18 KB, multiple of 16
+
+// Shared-memory map (identical offsets in both CTAs; barriers first).
+constexpr int kOffBars = 0;
+constexpr int kOffData = 2048;
+constexpr int kOffTiles = kOffData;                                   // kStages x 72 KB
+constexpr int kOffPBuf = kOffTiles + kStages * kKTileBytes;           // kPBufs x 18 KB
+constexpr int kOffF8 = kOffPBuf + kPBufs * kPBufBytes;                // 36 KB
+constexpr int kSmemBytesBf16 = kOffF8;
+constexpr int kSmemBytesFp8 = kOffF8 + kF8Bytes;
+constexpr int kSmemAlign = 1024;
+
+// TMEM columns.
+constexpr uint32_t kTmemQ = 0;       // score CTA: Q as A operand, 288 columns
+constexpr uint32_t kTmemS = 288;     // score CTA: two 64-column S buffers
+constexpr uint32_t kTmemO = 0;       // output CTA: O, 512 columns
+
+struct Bars {
+  uint64_t full[kStages];     // KV tile landed (TMA or fp8 conversion)
+  uint64_t empty[kStages];    // KV tile consumed by the MMA
+  uint64_t f8_full;           // fp8 staging landed
+  uint64_t f8_empty;          // fp8 staging converted
+  uint64_t s_full[2];         // score CTA: S tile computed
+  uint64_t s_free[2];         // score CTA: S tile read out
+  uint64_t q_full;            // score CTA: Q written to TMEM
+  uint64_t q_free;            // score CTA: all QK of the item done
+  uint64_t p_empty[kPBufs];   // score CTA: peer finished PV with P buffer
+  uint64_t p_ready[kPBufs];   // score CTA: the four softmax warps staged P
+  uint64_t p_full[kPBufs];    // output CTA: P buffer arrived
+  uint64_t corr_done[kPBufs]; // output CTA: O ready for PV on this P buffer
+  uint64_t o_ready[kPBufs];   // output CTA: PV with this P buffer complete
+  uint64_t o_free;            // output CTA: epilogue read O
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= kOffData, "barrier block too large");
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 128-byte swizzle: byte offset of 16-byte unit u of row r inside a chunk.
+__device__ __forceinline__ uint32_t swz(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
+
+// On a failed wait: record, raise the abort flag here and in the peer.
+__device__ __noinline__ void fail(Bars* bars, const DecodeParams& p, int site) {
+  record_error(p.ws_hdr, MLA_DEV_WAIT_TIMEOUT, site);
+  bars->abort = 1;
+  const uint32_t peer = cluster_rank() ^ 1u;
+  const uint32_t a = mapa(smem_u32(&bars->abort), peer);
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+}
+
+// Warp-collective bounded waits: every lane waits, and the warp leaves together
+// (to the teardown) if any lane gave up.
+#define WAIT(bar, par, site)                                                         \
+  if (!__all_sync(0xffffffffu, mbar_wait(bar, par, &bars->abort))) {               \
+    fail(bars, p, site);                                                             \
+    goto done;                                                                       \
+  }
+#define WAITC(bar, par, site)                                                        \
+  if (!__all_sync(0xffffffffu, mbar_wait<true>(bar, par, &bars->abort))) {         \
+    fail(bars, p, site);                                                             \
+    goto done;                                                                       \
+  }
+
+// Number of 64-entry tiles of an item.
+__device__ __forceinline__ int item_tiles(const Item& it) {
+  return it.ok && it.e1 > it.e0 ? (it.e1 - it.e0 + kBlockN - 1) / kBlockN : 0;
+}
+
+// Store 32 consecutive output columns of one row (bf16 or fp32).
+__device__ __forceinline__ void store_row32(const DecodeParams& p, float* dst_f32, int64_t row, int c0,
+                                            const float (&v)[32]) {
+  if (dst_f32 != nullptr) {
+    float4* d = reinterpret_cast<float4*>(dst_f32 + c0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) d[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row * kDv + c0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 u;
+      u.x = pack_bf16x2(v[8 * k + 0], v[8 * k + 1]);
+      u.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
+      u.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
+      u.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
+      d[k] = u;
+    }
+  }
+}
+
+// Split merge.  Each of the 4 row warps of every split fences its partial rows
+// and bumps the (request, group) counter; the warp that arrives last (4*S
+// arrivals) combines all splits in split order and writes the output.
+__device__ void merge_by_warp(const DecodeParams& p, const Item& it, int lane) {
+  __threadfence();
+  __syncwarp();
+  int last = 0;
+  if (lane == 0) last = atomicAdd(&p.counters[it.group], 1) == 4 * it.S - 1;
+  last = __shfl_sync(0xffffffffu, last, 0);
+  if (!last) return;
+  __threadfence();
+  const int B = p.batch;
+  const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
+  const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
+  const int nvec = it.nrows * (kDv / 4);
+  for (int v = lane; v < nvec; v += 32) {
+    const int r = v / (kDv / 4), d = (v % (kDv / 4)) * 4;
+    float M = -INFINITY;
+    for (int s = 0; s < it.S; ++s)
+      M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float tot = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < it.S; ++s) {
+        const int slot = pbase + s * G + it.g;
+        const float ls = __ldcg(p.part_lse + (int64_t)slot * kRows + r);
+        if (ls == -INFINITY) continue;
+        const float w = ex2((ls - M) * 1.4426950408889634f);
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + r) * kDv + d));
+        tot += w;
+        acc.x += w * o.x;
+        acc.y += w * o.y;
+        acc.z += w * o.z;
+        acc.w += w * o.w;
+      }
+      const float inv = 1.f / tot;
+      acc.x *= inv;
+      acc.y *= inv;
+      acc.z *= inv;
+      acc.w *= inv;
+    }
+    const int64_t row = it.q_row_base + it.row0 + r;
+    if (p.out_fp32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.o) + row * kDv + d) = acc;
+    } else {
+      uint2 u;
+      u.x = pack_bf16x2(acc.x, acc.y);
+      u.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * kDv + d) = u;
+    }
+    if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
+  }
+  if (lane == 0) p.counters[it.group] = 0;
+}
+
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = cluster_rank();
+  const bool score_cta = rank == 0;
+
+  if (!plan_header_ok(p.plan, p)) {
+    if (blockIdx.x == 0 && tid == 0) record_error(p.ws_hdr, MLA_DEV_PLAN_MISMATCH, 0);
+    return;   // both CTAs of every cluster leave before touching each other
+  }
+  const int n_items = p.plan[kHNItems];
+  const int cluster = (int)cluster_id_x(), n_clusters = (int)num_clusters_x();
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->full[s], kFp8 ? 4 : 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->f8_full, 1);
+    mbar_init(&bars->f8_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->s_full[b], 1);
+      mbar_init(&bars->s_free[b], 4);
+    }
+    mbar_init(&bars->q_full, 4);
+    mbar_init(&bars->q_free, 1);
+    for (int b = 0; b < kPBufs; ++b) {
+      mbar_init(&bars->p_empty[b], 1);
+      mbar_init(&bars->p_ready[b], 4);
+      mbar_init(&bars->p_full[b], 1);
+      mbar_init(&bars->corr_done[b], 4);
+      mbar_init(&bars->o_ready[b], 1);
+    }
+    mbar_init(&bars->o_free, 4);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap_kv);
+  fence_before_sync();
+  __syncthreads();
+  cluster_sync();        // barriers of both CTAs initialised before any remote arrival
+  fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  uint8_t* tiles = smem + kOffTiles;
+  uint8_t* pbufs = smem + kOffPBuf;
+  uint8_t* f8 = smem + kOffF8;
+  const int tile_bytes = score_cta ? kKTileBytes : kVTileBytes;
+  const int nchunks = score_cta ? 9 : 8;
+
+  // ======================================================================= producer
+  if (warp == kWarpProducer) {
+    uint32_t kseq = 0, f8seq = 0;
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages;
+        const uint32_t ph = (kseq / kStages) & 1;
+        // 64 slot indices of this tile; invalid or past-the-end entries read row -1 (zero fill).
+        int32_t r0, r1;
+        {
+          const int i0 = it.e0 + j * kBlockN + lane, i1 = i0 + 32;
+          r0 = -1;
+          r1 = -1;
+          if (i0 < it.e1) {
+            const int32_t s = __ldg(p.kv_indices + it.kv_off + i0);
+            if (s >= 0 && s < p.num_slots) r0 = s;
+            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i0));
+          }
+          if (i1 < it.e1) {
+            const int32_t s = __ldg(p.kv_indices + it.kv_off + i1);
+            if (s >= 0 && s < p.num_slots) r1 = s;
+            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i1));
+          }
+        }
+        if (!kFp8) {
+          WAIT(&bars->empty[st], ph ^ 1, 1);
+          uint8_t* dst = tiles + st * kKTileBytes;
+          if (lane == 0) mbar_arrive_expect_tx(&bars->full[st], (uint32_t)tile_bytes);
+          __syncwarp();
+          for (int g = 0; g < kBlockN / 4; ++g) {
+            // rows 4g..4g+3 live in lanes (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8)
+            const int src = (4 * g) & 31;
+            const int32_t a0 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src);
+            const int32_t a1 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 1);
+            const int32_t a2 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 2);
+            const int32_t a3 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 3);
+            if (lane < nchunks)
+              tma_gather4(smem_u32(dst + lane * kChunkBytes + g * 512), &tmap_kv, lane * 64, a0, a1, a2,
+                          a3, &bars->full[st]);
+          }
+        } else {
+          const uint32_t fph = f8seq & 1;
+          WAIT(&bars->f8_empty, fph ^ 1, 2);
+          if (lane == 0) mbar_arrive_expect_tx(&bars->f8_full, (uint32_t)(kBlockN * 192 * (score_cta ? 3 : 3)));
+          __syncwarp();
+          for (int g = 0; g < kBlockN / 4; ++g) {
+            const int src = (4 * g) & 31;
+            const int32_t a0 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src);
+            const int32_t a1 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 1);
+            const int32_t a2 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 2);
+            const int32_t a3 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 3);
+            // three 192-byte column chunks, each stored as [64 rows][192 B]
+            if (lane < 3)
+              tma_gather4(smem_u32(f8 + lane * (kBlockN * 192) + g * 4 * 192), &tmap_kv, lane * 192, a0,
+                          a1, a2, a3, &bars->f8_full);
+          }
+          ++f8seq;
+        }
+      }
+    }
+  }
+  // ======================================================================= fp8 conversion
+  else if (warp >= kWarpConv0) {
+    if (kFp8) {
+      const int ct = tid - kWarpConv0 * 32;   // 0..127
+      uint32_t kseq = 0, f8seq = 0;
+      for (int idx = cluster; idx < n_items; idx += n_clusters) {
+        const Item it = load_item(p, idx);
+        const int nt = item_tiles(it);
+        for (int j = 0; j < nt; ++j, ++kseq, ++f8seq) {
+          const int st = kseq % kStages;
+          const uint32_t ph = (kseq / kStages) & 1;
+          WAIT(&bars->f8_full, f8seq & 1, 3);
+          WAIT(&bars->empty[st], ph ^ 1, 4);
+          uint8_t* dst = tiles + st * kKTileBytes;
+          // unit = (entry e, 16-byte group of 16 fp8 values); nchunks*4 groups per entry
+          const int groups = nchunks * 4;
+          for (int u = ct; u < kBlockN * groups; u += 128) {
+            const int e = u / groups, gq = u % groups;      // gq: 16-column group
+            const int col = gq * 16;
+            const int cchunk = col / 192, cin = col % 192;
+            const uint4 raw = *reinterpret_cast<const uint4*>(f8 + cchunk * (kBlockN * 192) + e * 192 + cin);
+            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+            uint32_t outw[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              uint32_t h0, h1;
+              const uint16_t lo = (uint16_t)(w[k] & 0xFFFF), hi = (uint16_t)(w[k] >> 16);
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"(lo));
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"(hi));
+              // f16 bits -> bf16 bits with the same exponent field: value * 2^-112, exact
+              outw[2 * k] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
+              outw[2 * k + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
+            }
+            // 16 bf16 = two 16-byte units of the 64-column chunk col/64
+            const int chunk = col / 64, u0 = (col % 64) / 8;
+            uint8_t* base = dst + chunk * kChunkBytes;
+            *reinterpret_cast<uint4*>(base + swz(e, u0)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            *reinterpret_cast<uint4*>(base + swz(e, u0 + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->f8_empty);
+            mbar_arrive(&bars->full[st]);
+          }
+        }
+      }
+    }
+  }
+  // ======================================================================= score CTA: MMA
+  else if (score_cta && warp == kWarpMma) {
+    uint32_t kseq = 0, sseq = 0, qitem = 0;
+    const uint32_t idesc = idesc_bf16_f32(128, kBlockN, false, false);
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      if (nt == 0) continue;
+      WAIT(&bars->q_full, qitem & 1, 10);
+      fence_after_sync();
+      for (int j = 0; j < nt; ++j, ++kseq, ++sseq) {
+        const int st = kseq % kStages, sb = sseq & 1;
+        WAIT(&bars->s_free[sb], ((sseq >> 1) & 1) ^ 1, 11);
+        WAIT(&bars->full[st], (kseq / kStages) & 1, 12);
+        fence_after_sync();
+        if (lane == 0) {
+          const uint32_t kbase = smem_u32(tiles + st * kKTileBytes);
+          for (int k = 0; k < kDqk / 16; ++k) {
+            const uint64_t bdesc = smem_desc_sw128(kbase + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024);
+            mma_ts(tmem + kTmemS + sb * kBlockN, tmem + kTmemQ + 8 * k, bdesc, idesc, k > 0);
+          }
+          mma_commit(&bars->empty[st]);
+          mma_commit(&bars->s_full[sb]);
+        }
+        __syncwarp();
+      }
+      if (lane == 0) mma_commit(&bars->q_free);
+      __syncwarp();
+      ++qitem;
+    }
+  }
+  // ======================================================================= output CTA: MMA
+  else if (!score_cta && warp == kWarpMma) {
+    uint32_t kseq = 0, pseq = 0, oitem = 0;
+    const uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      if (nt == 0) continue;
+      WAIT(&bars->o_free, (oitem & 1) ^ 1, 20);
+      for (int j = 0; j < nt; ++j, ++kseq, ++pseq) {
+        const int st = kseq % kStages, pb = pseq % kPBufs;
+        const uint32_t pph = (pseq / kPBufs) & 1;
+        WAIT(&bars->full[st], (kseq / kStages) & 1, 21);
+        if (lane == 0) mbar_arrive_expect_tx(&bars->p_full[pb], kPBufBytes);
+        __syncwarp();
+        WAITC(&bars->p_full[pb], pph, 22);
+        WAIT(&bars->corr_done[pb], pph, 23);
+        fence_after_sync();
+        if (lane == 0) {
+          const uint32_t vbase = smem_u32(tiles + st * kKTileBytes);
+          const uint32_t pbase = smem_u32(pbufs + pb * kPBufBytes);
+          for (int h = 0; h < 2; ++h) {
+            for (int k = 0; k < kBlockN / 16; ++k) {
+              const uint64_t adesc = smem_desc_sw128(pbase + k * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(vbase + (4 * h) * kChunkBytes + k * 2048, kChunkBytes, 1024);
+              mma_ss(tmem + kTmemO + 256 * h, adesc, bdesc, idesc, (j > 0 || k > 0) ? 1u : 0u);
+            }
+          }
+          mma_commit(&bars->empty[st]);
+          mma_commit_mc(&bars->p_empty[pb], 0x1);
+          mma_commit(&bars->o_ready[pb]);
+        }
+        __syncwarp();
+      }
+      ++oitem;
+    }
+  }
+  // ======================================================================= score CTA: softmax
+  else if (score_cta) {
+    const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
+    const int r = 32 * q4 + lane;            // query row within the group
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    uint32_t sseq = 0, pseq = 0, qitem = 0;
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      if (nt == 0) continue;
+      const bool live = r < it.nrows;
+      // Q rows of the item -> TMEM (A operand layout: lane = row, two bf16 per column).
+      WAIT(&bars->q_free, (qitem & 1) ^ 1, 30);
+      fence_after_sync();
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                          (it.q_row_base + it.row0 + (live ? r : 0)) * kDqk);
+        for (int c = 0; c < 9; ++c) {
+          uint32_t v[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint4 u = live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+            v[4 * k] = u.x;
+            v[4 * k + 1] = u.y;
+            v[4 * k + 2] = u.z;
+            v[4 * k + 3] = u.w;
+          }
+          tmem_st32(tmem + lane_addr + kTmemQ + 32 * c, v);
+        }
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->q_full);
+      ++qitem;
+
+      // Visibility: local entry i is visible to this row iff i < iend and its index is valid.
+      int iend = it.e1;
+      if (p.causal && live) {
+        const int t = (it.row0 + r) / p.num_heads;
+        const int64_t lim = it.Lg - it.T + t - it.base;
+        const int64_t cnt = lim < 0 ? 0 : lim / it.stride + 1;
+        if (cnt < iend) iend = (int)cnt;
+      }
+      if (!live) iend = -1;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j, ++sseq, ++pseq) {
+        const int sb = sseq & 1, pb = pseq % kPBufs;
+        const int i0 = it.e0 + j * kBlockN;
+        // validity of the tile's 64 slot indices
+        uint32_t vlo, vhi;
+        {
+          const int a = i0 + lane, b = a + 32;
+          bool ok0 = false, ok1 = false;
+          if (a < it.e1) {
+            const int32_t s = __ldg(p.kv_indices + it.kv_off + a);
+            ok0 = s >= 0 && s < p.num_slots;
+          }
+          if (b < it.e1) {
+            const int32_t s = __ldg(p.kv_indices + it.kv_off + b);
+            ok1 = s >= 0 && s < p.num_slots;
+          }
+          vlo = __ballot_sync(0xffffffffu, ok0);
+          vhi = __ballot_sync(0xffffffffu, ok1);
+        }
+        WAIT(&bars->s_full[sb], (sseq >> 1) & 1, 31);
+        fence_after_sync();
+        uint32_t s0[32], s1[32];
+        tmem_ld32(tmem + lane_addr + kTmemS + sb * kBlockN, s0);
+        tmem_ld32(tmem + lane_addr + kTmemS + sb * kBlockN + 32, s1);
+        tmem_wait_ld();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+
+        const int nvis = iend - i0;   // entries [0, nvis) of the tile may be visible
+        float x[64];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          const uint32_t bits = e < 32 ? s0[e] : s1[e - 32];
+          const bool vis = e < nvis && (((e < 32 ? vlo : vhi) >> (e & 31)) & 1u);
+          x[e] = vis ? __uint_as_float(bits) * p.scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, x[e]);
+        }
+        float alpha = 1.f;
+        int need = 0;
+        if (tmax > m_ref + 8.f) {          // raise the reference max only when it grew a lot
+          alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - tmax);
+          m_ref = tmax;
+          need = 1;
+        }
+        float psum = 0.f;
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          const float a = m_ref == -INFINITY ? 0.f : ex2(x[e] - m_ref);
+          const float b = m_ref == -INFINITY ? 0.f : ex2(x[e + 1] - m_ref);
+          psum += a + b;
+          pk[e / 2] = pack_bf16x2(a, b);
+        }
+        l = l * alpha + psum;
+        const int any_need = __any_sync(0xffffffffu, need);
+
+        // Hand P to the output CTA.
+        WAITC(&bars->p_empty[pb], ((pseq / kPBufs) & 1) ^ 1, 32);
+        uint8_t* stg = pbufs + pb * kPBufBytes;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(stg + swz(r, u)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        float* stats = reinterpret_cast<float*>(stg + kPStatsOff);
+        stats[r] = alpha;
+        stats[128 + r] = m_ref;
+        stats[256 + r] = l;
+        if (lane == 0) reinterpret_cast<int*>(stats + 384)[q4] = any_need;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready[pb]);
+        if (warp == kWarpRow0) {
+          WAIT(&bars->p_ready[pb], (pseq / kPBufs) & 1, 34);
+          if (lane == 0) {
+            const uint32_t src = smem_u32(stg);
+            bulk_copy_to_peer(mapa(src, 1), src, kPBufBytes, mapa(smem_u32(&bars->p_full[pb]), 1));
+          }
+          __syncwarp();
+        }
+      }
+    }
+    // Drain: the peer's last PV arrivals on p_empty must land before this CTA exits.
+    for (int k = 0; k < kPBufs && (int)pseq - 1 - k >= 0; ++k) {
+      const uint32_t s = pseq - 1 - k;
+      WAITC(&bars->p_empty[s % kPBufs], (s / kPBufs) & 1, 33);
+    }
+  }
+  // ======================================================================= output CTA: correction + epilogue
+  else {
+    const int q4 = warp & 3;
+    const int r = 32 * q4 + lane;
+    const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    uint32_t pseq = 0;
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      if (!it.ok) continue;
+      const int nt = item_tiles(it);
+      const bool live = r < it.nrows;
+      float m_last = -INFINITY, l_last = 0.f;
+      for (int j = 0; j < nt; ++j, ++pseq) {
+        const int pb = pseq % kPBufs;
+        const uint32_t pph = (pseq / kPBufs) & 1;
+        WAITC(&bars->p_full[pb], pph, 40);
+        const uint8_t* pbuf = pbufs + pb * kPBufBytes;
+        const float* stats = reinterpret_cast<const float*>(pbuf + kPStatsOff);
+        const int* flags = reinterpret_cast<const int*>(stats + 384);
+        const float alpha = stats[r];
+        m_last = stats[128 + r];
+        l_last = stats[256 + r];
+        if (flags[q4] && j > 0) {
+          // O of the previous tile must be complete before rescaling it.
+          const uint32_t prev = pseq - 1;
+          WAIT(&bars->o_ready[prev % kPBufs], (prev / kPBufs) & 1, 41);
+          fence_after_sync();
+          for (int c = 0; c < kDv / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + kTmemO + 32 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
+            tmem_st32(tmem + lane_addr + kTmemO + 32 * c, v);
+          }
+          tmem_wait_st();
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->corr_done[pb]);
+      }
+      // Epilogue.
+      const bool any = l_last > 0.f;
+      const float inv = any ? p.out_scale / l_last : 0.f;
+      const float lse = any ? (m_last + __log2f(l_last)) * 0.69314718055994531f : -INFINITY;
+      float* dst_f32 = nullptr;
+      const int64_t row = it.q_row_base + it.row0 + r;
+      if (it.slot >= 0) dst_f32 = p.part_o + ((int64_t)it.slot * kRows + r) * kDv;
+      else if (p.out_fp32) dst_f32 = static_cast<float*>(p.o) + row * kDv;
+      if (nt > 0) {
+        const uint32_t last = pseq - 1;
+        WAIT(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
+        fence_after_sync();
+      }
+      for (int c = 0; c < kDv / 32; ++c) {
+        float v[32];
+        if (nt > 0) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_addr + kTmemO + 32 * c, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(u[k]) * inv;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        }
+        if (live) store_row32(p, dst_f32, row, 32 * c, v);
+      }
+      if (live) {
+        if (it.slot >= 0) p.part_lse[(int64_t)it.slot * kRows + r] = lse;
+        else p.lse[row] = lse;
+      }
+      if (nt > 0) {
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free);
+      }
+      if (it.slot >= 0) merge_by_warp(p, it, lane);
+    }
+  }
+
+done:
+  fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
+  cluster_sync();
+}
+
+// ----------------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+template <bool kFp8>
+mla_status launch_impl(const DecodeParams& dp, void* stream) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MLA_ERR_CUDA;
+  CUtensorMap tmap;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)dp.num_slots};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kDqk * (kFp8 ? 1 : 2)};
+  const cuuint32_t box[2] = {kFp8 ? 192u : 64u, 1u};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult cr = enc(&tmap, kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(dp.kv), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return MLA_ERR_INVALID_ARG;
+  const int smem = (kFp8 ? kSmemBytesFp8 : kSmemBytesBf16) + kSmemAlign;
+  auto kern = mla_decode_tensor_kernel<kFp8>;
+  static int configured[2] = {0, 0};
+  static int max_clusters[2] = {0, 0};
+  if (!configured[kFp8]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
+    max_clusters[kFp8] = n;
+    configured[kFp8] = 1;
+  }
+  int clusters = max_clusters[kFp8];
+  if (clusters > dp.items_cap) clusters = dp.items_cap > 0 ? dp.items_cap : 1;
+  DecodeParams kp = dp;
+  if (kFp8) {
+    // The in-register fp8 -> bf16 conversion scales every value by 2^-112.
+    kp.scale_log2 = dp.scale_log2 * 5.192296858534828e33f;
+    kp.out_scale = dp.out_scale * 5.192296858534828e33f;
+  }
+  kern<<<2 * clusters, kThreads, smem, (cudaStream_t)stream>>>(tmap, kp);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+int tensor_kernel_available() { return 1; }
+
+mla_status launch_decode_tensor(const DecodeParams& dp, void* stream) {
+  return dp.kv_fp8 ? launch_impl<true>(dp, stream) : launch_impl<false>(dp, stream);
+}
 
 }  // namespace mla
