@@ -75,7 +75,9 @@ constexpr uint32_t kTmemO = 0;       // output CTA: O, 512 columns
 
 struct Bars {
   uint64_t full[kStages];     // KV tile landed (TMA or fp8 conversion)
-  uint64_t empty[kStages];    // KV tile consumed by the MMA
+  uint64_t empty[kStages];    // KV tile consumed by this CTA's MMA
+  uint64_t pfree[kStages];    // bf16: the peer's MMA finished with its copy of the stage
+  uint64_t fwd[kStages];      // bf16: this CTA's half of the tile gathered, ready to forward
   uint64_t f8_full;           // fp8 staging landed
   uint64_t f8_empty;          // fp8 staging converted
   uint64_t s_full[2];         // score CTA: S tile computed
@@ -88,8 +90,14 @@ struct Bars {
   uint64_t corr_done[kPBufs]; // output CTA: O ready for PV on this P buffer
   uint64_t o_ready[kPBufs];   // output CTA: PV with this P buffer complete
   uint64_t o_free;            // output CTA: epilogue read O
+  uint64_t mrg_a;             // output CTA: the 4 row warps fenced their partial rows
+  uint64_t mrg_b;             // output CTA: leader published the last-arriver verdict
+  uint64_t mrg_c;             // output CTA: per-row merge weights ready
   uint32_t tmem_base;
   int abort;
+  int merge_last;
+  float merge_m[kRows];
+  float merge_inv[kRows];
 };
 static_assert(sizeof(Bars) <= kOffData, "barrier block too large");
 
@@ -111,7 +119,7 @@ __device__ __noinline__ void fail(Bars* bars, const DecodeParams& p, int site) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
 }
 
-// Warp-collective bounded waits: every lane waits, and the warp leaves together
+// Warp-collective bounded waits: every lane polls, and the warp leaves together
 // (to the teardown) if any lane gave up.
 #define WAIT(bar, par, site)                                                         \
   if (!__all_sync(0xffffffffu, mbar_wait(bar, par, &bars->abort))) {               \
@@ -150,61 +158,6 @@ __device__ __forceinline__ void store_row32(const DecodeParams& p, float* dst_f3
   }
 }
 
-// Split merge.  Each of the 4 row warps of every split fences its partial rows
-// and bumps the (request, group) counter; the warp that arrives last (4*S
-// arrivals) combines all splits in split order and writes the output.
-__device__ void merge_by_warp(const DecodeParams& p, const Item& it, int lane) {
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) last = atomicAdd(&p.counters[it.group], 1) == 4 * it.S - 1;
-  last = __shfl_sync(0xffffffffu, last, 0);
-  if (!last) return;
-  __threadfence();
-  const int B = p.batch;
-  const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
-  const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
-  const int nvec = it.nrows * (kDv / 4);
-  for (int v = lane; v < nvec; v += 32) {
-    const int r = v / (kDv / 4), d = (v % (kDv / 4)) * 4;
-    float M = -INFINITY;
-    for (int s = 0; s < it.S; ++s)
-      M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float tot = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < it.S; ++s) {
-        const int slot = pbase + s * G + it.g;
-        const float ls = __ldcg(p.part_lse + (int64_t)slot * kRows + r);
-        if (ls == -INFINITY) continue;
-        const float w = ex2((ls - M) * 1.4426950408889634f);
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + r) * kDv + d));
-        tot += w;
-        acc.x += w * o.x;
-        acc.y += w * o.y;
-        acc.z += w * o.z;
-        acc.w += w * o.w;
-      }
-      const float inv = 1.f / tot;
-      acc.x *= inv;
-      acc.y *= inv;
-      acc.z *= inv;
-      acc.w *= inv;
-    }
-    const int64_t row = it.q_row_base + it.row0 + r;
-    if (p.out_fp32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.o) + row * kDv + d) = acc;
-    } else {
-      uint2 u;
-      u.x = pack_bf16x2(acc.x, acc.y);
-      u.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + row * kDv + d) = u;
-    }
-    if (d == 0) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
-  }
-  if (lane == 0) p.counters[it.group] = 0;
-}
-
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p) {
@@ -224,8 +177,10 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], kFp8 ? 4 : 1);
+      mbar_init(&bars->full[s], kFp8 ? 4 : 2);
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->pfree[s], 1);
+      mbar_init(&bars->fwd[s], 1);
     }
     mbar_init(&bars->f8_full, 1);
     mbar_init(&bars->f8_empty, 4);
@@ -243,6 +198,9 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       mbar_init(&bars->o_ready[b], 1);
     }
     mbar_init(&bars->o_free, 4);
+    mbar_init(&bars->mrg_a, 4);
+    mbar_init(&bars->mrg_b, 1);
+    mbar_init(&bars->mrg_c, 4);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -263,7 +221,18 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   const int nchunks = score_cta ? 9 : 8;
 
   // ======================================================================= producer
-  if (warp == kWarpProducer) {
+  // bf16: each CTA gathers half of every KV tile and forwards it to the peer with
+  // one bulk copy (row gathers are the per-SM bottleneck, bulk copies are not):
+  //   score CTA gathers chunks 0-3 (forwarded) and 8 (RoPE, kept);
+  //   output CTA gathers chunks 4-7 (forwarded).
+  // Warps 0, 6, 7 and 9 gather (one per SM sub-partition: TMA issue throughput
+  // scales with the number of sub-partitions issuing); warp 8 forwards.
+  // fp8: warp 0 gathers the whole fp8 tile; the conversion warps convert it.
+  if (warp == kWarpProducer ||
+      (!kFp8 && (warp == kWarpConv0 || warp == kWarpConv0 + 1 || warp == kWarpConv0 + 3))) {
+    const int pw = warp == kWarpProducer ? 0 : (warp == kWarpConv0 + 3 ? 3 : warp - kWarpConv0 + 1);
+    constexpr int npw = kFp8 ? 1 : 4;
+    const int nown = score_cta ? 5 : 4;                 // chunks this CTA gathers
     uint32_t kseq = 0, f8seq = 0;
     for (int idx = cluster; idx < n_items; idx += n_clusters) {
       const Item it = load_item(p, idx);
@@ -277,32 +246,39 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
           const int i0 = it.e0 + j * kBlockN + lane, i1 = i0 + 32;
           r0 = -1;
           r1 = -1;
+          const bool report = score_cta && pw == 0;
           if (i0 < it.e1) {
             const int32_t s = __ldg(p.kv_indices + it.kv_off + i0);
             if (s >= 0 && s < p.num_slots) r0 = s;
-            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i0));
+            else if (report) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i0));
           }
           if (i1 < it.e1) {
             const int32_t s = __ldg(p.kv_indices + it.kv_off + i1);
             if (s >= 0 && s < p.num_slots) r1 = s;
-            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i1));
+            else if (report) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i1));
           }
         }
         if (!kFp8) {
           WAIT(&bars->empty[st], ph ^ 1, 1);
           uint8_t* dst = tiles + st * kKTileBytes;
-          if (lane == 0) mbar_arrive_expect_tx(&bars->full[st], (uint32_t)tile_bytes);
+          if (pw == 0 && lane == 0) {
+            // full: own direct chunk (score: RoPE) + the peer's forwarded half
+            mbar_arrive_expect_tx(&bars->full[st], (uint32_t)((score_cta ? 1 : 0) * kChunkBytes + 4 * kChunkBytes));
+            mbar_arrive_expect_tx(&bars->fwd[st], (uint32_t)(4 * kChunkBytes));
+          }
           __syncwarp();
-          for (int g = 0; g < kBlockN / 4; ++g) {
+          for (int op = pw; op < nown * (kBlockN / 4); op += npw) {
+            const int k = op / (kBlockN / 4), g = op % (kBlockN / 4);
+            const int c = score_cta ? (k < 4 ? k : 8) : 4 + k;
             // rows 4g..4g+3 live in lanes (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8)
             const int src = (4 * g) & 31;
             const int32_t a0 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src);
             const int32_t a1 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 1);
             const int32_t a2 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 2);
             const int32_t a3 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 3);
-            if (lane < nchunks)
-              tma_gather4(smem_u32(dst + lane * kChunkBytes + g * 512), &tmap_kv, lane * 64, a0, a1, a2,
-                          a3, &bars->full[st]);
+            if (lane == 0)
+              tma_gather4(smem_u32(dst + c * kChunkBytes + g * 512), &tmap_kv, c * 64, a0, a1, a2, a3,
+                          c == 8 ? &bars->full[st] : &bars->fwd[st]);
           }
         } else {
           const uint32_t fph = f8seq & 1;
@@ -323,6 +299,33 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
           ++f8seq;
         }
       }
+    }
+  }
+  // ======================================================================= bf16: forward half tiles
+  else if (!kFp8 && warp == kWarpConv0 + 2) {
+    uint32_t kseq = 0;
+    const uint32_t half_off = score_cta ? 0u : (uint32_t)(4 * kChunkBytes);
+    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages;
+        WAIT(&bars->fwd[st], (kseq / kStages) & 1, 5);
+        WAITC(&bars->pfree[st], ((kseq / kStages) & 1) ^ 1, 7);
+        if (lane == 0) {
+          const uint32_t src = smem_u32(tiles + st * kKTileBytes) + half_off;
+          const uint32_t peer = rank ^ 1u;
+          bulk_copy_to_peer(mapa(src, peer), src, 4 * kChunkBytes, mapa(smem_u32(&bars->full[st]), peer));
+          mbar_arrive(&bars->full[st]);
+        }
+        __syncwarp();
+      }
+    }
+    // The peer's last multicast commits target this CTA's barriers: they must
+    // land before this CTA exits.
+    for (int k = 0; k < kStages && (int)kseq - 1 - k >= 0; ++k) {
+      const uint32_t s2 = kseq - 1 - k;
+      WAITC(&bars->pfree[s2 % kStages], (s2 / kStages) & 1, 6);
     }
   }
   // ======================================================================= fp8 conversion
@@ -387,7 +390,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       for (int j = 0; j < nt; ++j, ++kseq, ++sseq) {
         const int st = kseq % kStages, sb = sseq & 1;
         WAIT(&bars->s_free[sb], ((sseq >> 1) & 1) ^ 1, 11);
-        WAIT(&bars->full[st], (kseq / kStages) & 1, 12);
+        WAITC(&bars->full[st], (kseq / kStages) & 1, 12);
         fence_after_sync();
         if (lane == 0) {
           const uint32_t kbase = smem_u32(tiles + st * kKTileBytes);
@@ -396,6 +399,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
             mma_ts(tmem + kTmemS + sb * kBlockN, tmem + kTmemQ + 8 * k, bdesc, idesc, k > 0);
           }
           mma_commit(&bars->empty[st]);
+          if (!kFp8) mma_commit_mc(&bars->pfree[st], 0x2);
           mma_commit(&bars->s_full[sb]);
         }
         __syncwarp();
@@ -417,7 +421,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       for (int j = 0; j < nt; ++j, ++kseq, ++pseq) {
         const int st = kseq % kStages, pb = pseq % kPBufs;
         const uint32_t pph = (pseq / kPBufs) & 1;
-        WAIT(&bars->full[st], (kseq / kStages) & 1, 21);
+        WAITC(&bars->full[st], (kseq / kStages) & 1, 21);
         if (lane == 0) mbar_arrive_expect_tx(&bars->p_full[pb], kPBufBytes);
         __syncwarp();
         WAITC(&bars->p_full[pb], pph, 22);
@@ -434,6 +438,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
             }
           }
           mma_commit(&bars->empty[st]);
+          if (!kFp8) mma_commit_mc(&bars->pfree[st], 0x1);
           mma_commit_mc(&bars->p_empty[pb], 0x1);
           mma_commit(&bars->o_ready[pb]);
         }
@@ -459,17 +464,24 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                           (it.q_row_base + it.row0 + (live ? r : 0)) * kDqk);
-        for (int c = 0; c < 9; ++c) {
-          uint32_t v[32];
+        // 72 loads of 16 bytes per row: issue 24 at a time (three TMEM chunks) to
+        // overlap the global-memory latency.
+        for (int c0 = 0; c0 < 9; c0 += 3) {
+          uint4 u[24];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint4 u = live ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
-            v[4 * k] = u.x;
-            v[4 * k + 1] = u.y;
-            v[4 * k + 2] = u.z;
-            v[4 * k + 3] = u.w;
+          for (int k = 0; k < 24; ++k) u[k] = live ? __ldg(src + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int cc = 0; cc < 3; ++cc) {
+            uint32_t v[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] = u[8 * cc + k].x;
+              v[4 * k + 1] = u[8 * cc + k].y;
+              v[4 * k + 2] = u[8 * cc + k].z;
+              v[4 * k + 3] = u[8 * cc + k].w;
+            }
+            tmem_st32(tmem + lane_addr + kTmemQ + 32 * (c0 + cc), v);
           }
-          tmem_st32(tmem + lane_addr + kTmemQ + 32 * c, v);
         }
         tmem_wait_st();
       }
@@ -581,7 +593,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    uint32_t pseq = 0;
+    uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0;
     for (int idx = cluster; idx < n_items; idx += n_clusters) {
       const Item it = load_item(p, idx);
       if (!it.ok) continue;
@@ -653,7 +665,94 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->o_free);
       }
-      if (it.slot >= 0) merge_by_warp(p, it, lane);
+      if (it.slot >= 0) {
+        // Fused split merge: the last split of this (request, row group) to finish
+        // combines every split's partial in split order.  The 4 row warps first
+        // agree (leader counts one arrival per split), then merge together.
+        __threadfence();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->mrg_a);
+        if (warp == kWarpRow0) {
+          WAIT(&bars->mrg_a, mrg_a_ph, 43);
+          if (lane == 0) {
+            bars->merge_last = atomicAdd(&p.counters[it.group], 1) == it.S - 1;
+            mbar_arrive(&bars->mrg_b);
+          }
+          __syncwarp();
+        }
+        mrg_a_ph ^= 1;
+        WAIT(&bars->mrg_b, mrg_b_ph, 44);
+        mrg_b_ph ^= 1;
+        if (bars->merge_last) {
+          __threadfence();
+          const int B = p.batch;
+          const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
+          const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
+          // pass 1: per-row max and normaliser (thread = row)
+          if (live) {
+            float M = -INFINITY;
+            for (int s = 0; s < it.S; ++s)
+              M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
+            float tot = 0.f;
+            if (M != -INFINITY)
+              for (int s = 0; s < it.S; ++s) {
+                const float ls = __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r);
+                tot += ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
+              }
+            bars->merge_m[r] = M;
+            bars->merge_inv[r] = M == -INFINITY ? 0.f : 1.f / tot;
+            p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->mrg_c);
+          WAIT(&bars->mrg_c, mrg_c_ph, 45);
+          mrg_c_ph ^= 1;
+          // pass 2: thread t owns float4 column t of every row; 8 rows in flight
+          const int c4 = tid - kWarpRow0 * 32;
+          for (int rb = 0; rb < it.nrows; rb += 8) {
+            float4 acc[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s = 0; s < it.S; ++s) {
+              const int slot = pbase + s * G + it.g;
+              float ls[8];
+              float4 ov[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rr = min(rb + k, it.nrows - 1);
+                ls[k] = __ldcg(p.part_lse + (int64_t)slot * kRows + rr);
+                ov[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + rr) * kDv) + c4);
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int rr = min(rb + k, it.nrows - 1);
+                const float M = bars->merge_m[rr];
+                const float w = (ls[k] == -INFINITY || M == -INFINITY) ? 0.f
+                                : ex2((ls[k] - M) * 1.4426950408889634f) * bars->merge_inv[rr];
+                acc[k].x += w * ov[k].x;
+                acc[k].y += w * ov[k].y;
+                acc[k].z += w * ov[k].z;
+                acc[k].w += w * ov[k].w;
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              if (rb + k >= it.nrows) break;
+              const int64_t orow = it.q_row_base + it.row0 + rb + k;
+              if (p.out_fp32) {
+                reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * kDv)[c4] = acc[k];
+              } else {
+                uint2 u;
+                u.x = pack_bf16x2(acc[k].x, acc[k].y);
+                u.y = pack_bf16x2(acc[k].z, acc[k].w);
+                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * kDv)[c4] = u;
+              }
+            }
+          }
+          if (tid == kWarpRow0 * 32) p.counters[it.group] = 0;
+        }
+      }
     }
   }
 
