@@ -201,6 +201,25 @@ mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const fl
  * *info its detail; returns MLA_ERR_DEVICE_FAULT when *code != 0. */
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info);
 
+/* Forward call for callers that cannot allocate device memory (a runtime or
+ * allocator that hands out only input and output tensors): the plan buffer and
+ * the workspace come from one static device array of 16 MiB inside the library
+ * instead of the caller.  The pages have no counterpart; it is a deployment
+ * convenience.  Arguments are those of mla_decode_fwd, except that plan_d,
+ * plan_bytes, workspace_d and ws_bytes are ignored.
+ *   - DYNAMIC mode only (the plan is rebuilt on the device by every call);
+ *     another mode returns MLA_ERR_UNSUPPORTED.
+ *   - Problems whose plan plus workspace exceed 16 MiB return
+ *     MLA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   - Allocates nothing.  The first call on a device looks up that device's
+ *     copy of the array (cudaGetSymbolAddress); make it before any stream
+ *     capture.  The array stays resident while the library is loaded.
+ *   - All calls share the array: calls that overlap on the GPU race on it.
+ *     Each call clears the state that must start at zero.
+ *   - Device-side faults are recorded in the array's error word, which this ABI
+ *     does not expose. */
+mla_status mla_decode_fwd_noalloc(const mla_fwd_args* args, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

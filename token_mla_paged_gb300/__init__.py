@@ -71,6 +71,7 @@ def _load():
         "mla_decode_plan": (ctypes.c_int, [pp, vp, vp, vp, sz]),
         "mla_decode_plan_device": (ctypes.c_int, [pp, vp, vp, vp, sz, vp, sz, vp]),
         "mla_decode_fwd": (ctypes.c_int, [ctypes.POINTER(FwdArgs), vp]),
+        "mla_decode_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FwdArgs), vp]),
         "mla_merge_states": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, i32, vp, vp]),
         "mla_get_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
     }
@@ -86,7 +87,7 @@ _lib = _load()
 # Symbols the header declares; tests check the library exports each one.
 ABI_SYMBOLS = ("mla_abi_version", "mla_status_string", "mla_decode_plan_size", "mla_decode_plan",
                "mla_decode_plan_device", "mla_decode_fwd", "mla_merge_states",
-               "mla_get_device_error")
+               "mla_get_device_error", "mla_decode_fwd_noalloc")
 
 
 def library():
