@@ -53,7 +53,6 @@ constexpr int kPBufs = 2;              // P hand-off ring
 constexpr int kChunkBytes = kBlockN * 128;          // 64 entries x 64 bf16 columns = 8 KB
 constexpr int kKTileBytes = 9 * kChunkBytes;        // 576 columns (score CTA)
 constexpr int kVTileBytes = 8 * kChunkBytes;        // 512 columns (output CTA)
-constexpr int kF8Bytes = kBlockN * kDqk;            // fp8 staging, 64 x 576 bytes
 constexpr int kPBytes = kRows * 128;                // P: 128 rows x 64 bf16
 constexpr int kPStatsOff = kPBytes;                 // alpha[128], m[128], l[128], flags[4]
 constexpr int kPBufBytes = kPBytes + 3 * 512 + 512; // 18 KB, multiple of 16
@@ -63,9 +62,7 @@ constexpr int kOffBars = 0;
 constexpr int kOffData = 2048;
 constexpr int kOffTiles = kOffData;                                   // kStages x 72 KB
 constexpr int kOffPBuf = kOffTiles + kStages * kKTileBytes;           // kPBufs x 18 KB
-constexpr int kOffF8 = kOffPBuf + kPBufs * kPBufBytes;                // 36 KB
-constexpr int kSmemBytesBf16 = kOffF8;
-constexpr int kSmemBytesFp8 = kOffF8 + kF8Bytes;
+constexpr int kSmemBytes = kOffPBuf + kPBufs * kPBufBytes;
 constexpr int kSmemAlign = 1024;
 
 // TMEM columns.
@@ -78,8 +75,6 @@ struct Bars {
   uint64_t empty[kStages];    // KV tile consumed by this CTA's MMA
   uint64_t pfree[kStages];    // bf16: the peer's MMA finished with its copy of the stage
   uint64_t fwd[kStages];      // bf16: this CTA's half of the tile gathered, ready to forward
-  uint64_t f8_full;           // fp8 staging landed
-  uint64_t f8_empty;          // fp8 staging converted
   uint64_t s_full[2];         // score CTA: S tile computed
   uint64_t s_free[2];         // score CTA: S tile read out
   uint64_t q_full;            // score CTA: Q written to TMEM
@@ -132,6 +127,14 @@ __device__ __noinline__ void fail(Bars* bars, const DecodeParams& p, int site) {
     goto done;                                                                       \
   }
 
+// Static work assignment, identical in every role of both CTAs of a cluster:
+// round r gives cluster c item r*C + c on even rounds and r*C + (C-1-c) on odd
+// rounds, so a cost-sorted item list is dealt out boustrophedon-fashion.
+__device__ __forceinline__ int item_of(int r, int c, int C) { return r * C + ((r & 1) ? C - 1 - c : c); }
+#define FOR_ITEMS(idx)                                                      \
+  for (int r_ = 0, idx = item_of(0, cluster, n_clusters); idx < n_items; \
+       ++r_, idx = item_of(r_, cluster, n_clusters))
+
 // Number of 64-entry tiles of an item.
 __device__ __forceinline__ int item_tiles(const Item& it) {
   return it.ok && it.e1 > it.e0 ? (it.e1 - it.e0 + kBlockN - 1) / kBlockN : 0;
@@ -182,8 +185,6 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       mbar_init(&bars->pfree[s], 1);
       mbar_init(&bars->fwd[s], 1);
     }
-    mbar_init(&bars->f8_full, 1);
-    mbar_init(&bars->f8_empty, 4);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
       mbar_init(&bars->s_free[b], 4);
@@ -216,7 +217,6 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   const uint32_t tmem = bars->tmem_base;
   uint8_t* tiles = smem + kOffTiles;
   uint8_t* pbufs = smem + kOffPBuf;
-  uint8_t* f8 = smem + kOffF8;
   const int tile_bytes = score_cta ? kKTileBytes : kVTileBytes;
   const int nchunks = score_cta ? 9 : 8;
 
@@ -228,13 +228,13 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   // Warps 0, 6, 7 and 9 gather (one per SM sub-partition: TMA issue throughput
   // scales with the number of sub-partitions issuing); warp 8 forwards.
   // fp8: warp 0 gathers the whole fp8 tile; the conversion warps convert it.
-  if (warp == kWarpProducer ||
-      (!kFp8 && (warp == kWarpConv0 || warp == kWarpConv0 + 1 || warp == kWarpConv0 + 3))) {
+  if (!kFp8 && (warp == kWarpProducer || warp == kWarpConv0 || warp == kWarpConv0 + 1 ||
+                warp == kWarpConv0 + 3)) {
     const int pw = warp == kWarpProducer ? 0 : (warp == kWarpConv0 + 3 ? 3 : warp - kWarpConv0 + 1);
     constexpr int npw = kFp8 ? 1 : 4;
     const int nown = score_cta ? 5 : 4;                 // chunks this CTA gathers
-    uint32_t kseq = 0, f8seq = 0;
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    uint32_t kseq = 0;
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       for (int j = 0; j < nt; ++j, ++kseq) {
@@ -280,32 +280,18 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
               tma_gather4(smem_u32(dst + c * kChunkBytes + g * 512), &tmap_kv, c * 64, a0, a1, a2, a3,
                           c == 8 ? &bars->full[st] : &bars->fwd[st]);
           }
-        } else {
-          const uint32_t fph = f8seq & 1;
-          WAIT(&bars->f8_empty, fph ^ 1, 2);
-          if (lane == 0) mbar_arrive_expect_tx(&bars->f8_full, (uint32_t)(kBlockN * 192 * (score_cta ? 3 : 3)));
-          __syncwarp();
-          for (int g = 0; g < kBlockN / 4; ++g) {
-            const int src = (4 * g) & 31;
-            const int32_t a0 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src);
-            const int32_t a1 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 1);
-            const int32_t a2 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 2);
-            const int32_t a3 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 3);
-            // three 192-byte column chunks, each stored as [64 rows][192 B]
-            if (lane < 3)
-              tma_gather4(smem_u32(f8 + lane * (kBlockN * 192) + g * 4 * 192), &tmap_kv, lane * 192, a0,
-                          a1, a2, a3, &bars->f8_full);
-          }
-          ++f8seq;
         }
       }
     }
+  }
+  // ======================================================================= fp8: warp 0 has no job
+  else if (warp == kWarpProducer) {
   }
   // ======================================================================= bf16: forward half tiles
   else if (!kFp8 && warp == kWarpConv0 + 2) {
     uint32_t kseq = 0;
     const uint32_t half_off = score_cta ? 0u : (uint32_t)(4 * kChunkBytes);
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       for (int j = 0; j < nt; ++j, ++kseq) {
@@ -328,52 +314,69 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       WAITC(&bars->pfree[s2 % kStages], (s2 / kStages) & 1, 6);
     }
   }
-  // ======================================================================= fp8 conversion
-  else if (warp >= kWarpConv0) {
-    if (kFp8) {
-      const int ct = tid - kWarpConv0 * 32;   // 0..127
-      uint32_t kseq = 0, f8seq = 0;
-      for (int idx = cluster; idx < n_items; idx += n_clusters) {
-        const Item it = load_item(p, idx);
-        const int nt = item_tiles(it);
-        for (int j = 0; j < nt; ++j, ++kseq, ++f8seq) {
-          const int st = kseq % kStages;
-          const uint32_t ph = (kseq / kStages) & 1;
-          WAIT(&bars->f8_full, f8seq & 1, 3);
-          WAIT(&bars->empty[st], ph ^ 1, 4);
-          uint8_t* dst = tiles + st * kKTileBytes;
-          // unit = (entry e, 16-byte group of 16 fp8 values); nchunks*4 groups per entry
-          const int groups = nchunks * 4;
-          for (int u = ct; u < kBlockN * groups; u += 128) {
-            const int e = u / groups, gq = u % groups;      // gq: 16-column group
-            const int col = gq * 16;
-            const int cchunk = col / 192, cin = col % 192;
-            const uint4 raw = *reinterpret_cast<const uint4*>(f8 + cchunk * (kBlockN * 192) + e * 192 + cin);
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-            uint32_t outw[8];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              uint32_t h0, h1;
-              const uint16_t lo = (uint16_t)(w[k] & 0xFFFF), hi = (uint16_t)(w[k] >> 16);
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"(lo));
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"(hi));
-              // f16 bits -> bf16 bits with the same exponent field: value * 2^-112, exact
-              outw[2 * k] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
-              outw[2 * k + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
-            }
-            // 16 bf16 = two 16-byte units of the 64-column chunk col/64
-            const int chunk = col / 64, u0 = (col % 64) / 8;
-            uint8_t* base = dst + chunk * kChunkBytes;
-            *reinterpret_cast<uint4*>(base + swz(e, u0)) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-            *reinterpret_cast<uint4*>(base + swz(e, u0 + 1)) = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&bars->f8_empty);
-            mbar_arrive(&bars->full[st]);
+  // ======================================================================= fp8: load + convert
+  // The four conversion warps read the indexed fp8 rows straight from global
+  // memory (16-byte loads, all issued before waiting for the stage), convert
+  // them in registers and write the swizzled bf16 tile.  Warp cw owns rows
+  // 16cw .. 16cw+15 of every tile.
+  else if (kFp8 && warp >= kWarpConv0) {
+    const int cw = warp - kWarpConv0;
+    const int units = score_cta ? kDqk / 16 : kDv / 16;   // 16-byte fp8 units per row
+    const int per = 16 * units / 32;                       // units per lane per tile
+    const uint8_t* pool = static_cast<const uint8_t*>(p.kv);
+    uint32_t kseq = 0;
+    FOR_ITEMS(idx) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages;
+        const uint32_t ph = (kseq / kStages) & 1;
+        int32_t myslot = -1;
+        if (lane < 16) {
+          const int i = it.e0 + j * kBlockN + 16 * cw + lane;
+          if (i < it.e1) {
+            const int32_t sl = __ldg(p.kv_indices + it.kv_off + i);
+            if (sl >= 0 && sl < p.num_slots) myslot = sl;
+            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
           }
         }
+        uint4 raw[kDqk / 32];
+#pragma unroll
+        for (int k = 0; k < kDqk / 32; ++k) {
+          raw[k] = make_uint4(0, 0, 0, 0);
+          if (k < per) {
+            const int flat = k * 32 + lane, e = flat / units, u = flat % units;
+            const int32_t sl = __shfl_sync(0xffffffffu, myslot, e);
+            if (sl >= 0) raw[k] = __ldg(reinterpret_cast<const uint4*>(pool + (int64_t)sl * kDqk + u * 16));
+          }
+        }
+        WAIT(&bars->empty[st], ph ^ 1, 4);
+        uint8_t* dst = tiles + st * kKTileBytes;
+#pragma unroll
+        for (int k = 0; k < kDqk / 32; ++k) {
+          if (k < per) {
+            const int flat = k * 32 + lane, e = 16 * cw + flat / units, u = flat % units;
+            const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t h0, h1;
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)(w[q] & 0xFFFF)));
+              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)(w[q] >> 16)));
+              // f16 bits -> bf16 bits with the same exponent field: value * 2^-112, exact
+              o[2 * q] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
+              o[2 * q + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
+            }
+            // 16 values = two 16-byte units of 64-column chunk u/4
+            uint8_t* base = dst + (u >> 2) * kChunkBytes;
+            const int u0 = (u & 3) * 2;
+            *reinterpret_cast<uint4*>(base + swz(e, u0)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(base + swz(e, u0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->full[st]);
       }
     }
   }
@@ -381,7 +384,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   else if (score_cta && warp == kWarpMma) {
     uint32_t kseq = 0, sseq = 0, qitem = 0;
     const uint32_t idesc = idesc_bf16_f32(128, kBlockN, false, false);
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
@@ -413,7 +416,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   else if (!score_cta && warp == kWarpMma) {
     uint32_t kseq = 0, pseq = 0, oitem = 0;
     const uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
@@ -453,7 +456,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     const int r = 32 * q4 + lane;            // query row within the group
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     uint32_t sseq = 0, pseq = 0, qitem = 0;
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
@@ -594,7 +597,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0;
-    for (int idx = cluster; idx < n_items; idx += n_clusters) {
+    FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       if (!it.ok) continue;
       const int nt = item_tiles(it);
@@ -796,7 +799,7 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
                     kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return MLA_ERR_INVALID_ARG;
-  const int smem = (kFp8 ? kSmemBytesFp8 : kSmemBytesBf16) + kSmemAlign;
+  const int smem = kSmemBytes + kSmemAlign;
   auto kern = mla_decode_tensor_kernel<kFp8>;
   static int configured[2] = {0, 0};
   static int max_clusters[2] = {0, 0};
