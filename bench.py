@@ -79,6 +79,20 @@ def algorithmic_bytes(w) -> int:
     return nnz * 576 * elem + 4 * nnz + rows * (576 * 2 + 512 * 2 + 4)
 
 
+def ncu_traffic(config: str):
+    """DRAM bytes of one decode launch from the committed ncu capture, only if the
+    kernel source is the one that was profiled; else None."""
+    import hashlib
+    try:
+        d = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+        src = open(os.path.join(ROOT, d["kernel_source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest()[:16] != d["kernel_source_sha256_16"]:
+            return None
+        return d["workloads"].get(config, {}).get("dram_bytes")
+    except Exception:
+        return None
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -204,6 +218,25 @@ def _single_request(w, b):
             [0, int(w.g_kv_indptr[b + 1] - w.g_kv_indptr[b])], np.int32))
 
 
+# ----------------------------------------------------------------------------- multi-rank timing
+
+def slowest_rank_ms(ms: float, world: int, device="cpu") -> float:
+    """Max over ranks of a per-rank time (no-op on one rank)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_slowest: float) -> float:
+    """Weak scaling: every rank decodes its own batch of the same shape, so the job
+    processes world * units in the slowest rank's time."""
+    return world * units_per_rank / (ms_slowest * 1e-3)
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -317,10 +350,7 @@ def main():
         torch.distributed.barrier()
     times = [a.elapsed_time(b) for a, b in evs]
     ms = sum(times) / len(times)
-    ms_t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = slowest_rank_ms(ms, world, device="cuda")
 
     # End to end through the public API: host (pinned) q + index lists in, O + LSE out.
     q_h = dev["q"].cpu().pin_memory()
@@ -343,11 +373,7 @@ def main():
         l_h.copy_(out_final[1], non_blocking=True)
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
-    e2e_t = torch.tensor([e2e_ms], device="cuda")
-    if world > 1:
-        torch.distributed.all_reduce(e2e_t, op=torch.distributed.ReduceOp.MAX)
-    e2e_ms = float(e2e_t.item())
+    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps, world, device="cuda")
 
     peaks = load_peaks()
     achieved_tf = flops / (ms * 1e-3) / 1e12
@@ -360,7 +386,7 @@ def main():
             cpu = {"value": u / s, "unit": "KV-tokens*heads/s", "cores": cores, "kind": "oracle",
                    "sample": f"{done} whole request(s) of the same workload, {s:.1f} s"}
         line = {
-            "metric": METRIC, "value": world * units / (ms_max * 1e-3), "unit": "KV-tokens*heads/s",
+            "metric": METRIC, "value": whole_job_rate(units, world, ms_max), "unit": "KV-tokens*heads/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-kv/bf16-mma",
@@ -370,12 +396,13 @@ def main():
                        "kv_dtype": w.kv_dtype, "causal": w.causal, "plan": "static" if extra["mode"] == 0 else "dynamic",
                        "algo": args.algo, "workers": workers, "l2": "flushed (256 MB write) between timed steps"},
             "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"], "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
+                         "traffic": ncu_traffic(args.config) if args.algo == "tensor" else None,
                          "peak_source": peaks["source"], "hbm_achieved_gbs": achieved_gbs,
                          "hbm_frac": achieved_gbs / peaks["hbm_gbs"], "alg_flops": flops,
                          "alg_bytes": nbytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": world * units / (e2e_ms * 1e-3), "unit": "KV-tokens*heads/s",
+            "e2e": {"value": whole_job_rate(units, world, e2e_ms), "unit": "KV-tokens*heads/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(),
