@@ -52,7 +52,6 @@ constexpr int kPBufs = 2;              // P hand-off ring
 
 constexpr int kChunkBytes = kBlockN * 128;          // 64 entries x 64 bf16 columns = 8 KB
 constexpr int kKTileBytes = 9 * kChunkBytes;        // 576 columns (score CTA)
-constexpr int kVTileBytes = 8 * kChunkBytes;        // 512 columns (output CTA)
 constexpr int kPBytes = kRows * 128;                // P: 128 rows x 64 bf16
 constexpr int kPStatsOff = kPBytes;                 // alpha[128], m[128], l[128], flags[4]
 constexpr int kPBufBytes = kPBytes + 3 * 512 + 512; // 18 KB, multiple of 16
@@ -73,8 +72,6 @@ constexpr uint32_t kTmemO = 0;       // output CTA: O, 512 columns
 struct Bars {
   uint64_t full[kStages];     // KV tile landed (TMA or fp8 conversion)
   uint64_t empty[kStages];    // KV tile consumed by this CTA's MMA
-  uint64_t pfree[kStages];    // bf16: the peer's MMA finished with its copy of the stage
-  uint64_t fwd[kStages];      // bf16: this CTA's half of the tile gathered, ready to forward
   uint64_t s_full[2];         // score CTA: S tile computed
   uint64_t s_free[2];         // score CTA: S tile read out
   uint64_t q_full;            // score CTA: Q written to TMEM
@@ -180,10 +177,8 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], kFp8 ? 4 : 2);
+      mbar_init(&bars->full[s], kFp8 ? 4 : 1);
       mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->pfree[s], 1);
-      mbar_init(&bars->fwd[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -217,69 +212,66 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   const uint32_t tmem = bars->tmem_base;
   uint8_t* tiles = smem + kOffTiles;
   uint8_t* pbufs = smem + kOffPBuf;
-  const int tile_bytes = score_cta ? kKTileBytes : kVTileBytes;
   const int nchunks = score_cta ? 9 : 8;
 
   // ======================================================================= producer
-  // bf16: each CTA gathers half of every KV tile and forwards it to the peer with
-  // one bulk copy (row gathers are the per-SM bottleneck, bulk copies are not):
-  //   score CTA gathers chunks 0-3 (forwarded) and 8 (RoPE, kept);
-  //   output CTA gathers chunks 4-7 (forwarded).
-  // Warps 0, 6, 7 and 9 gather (one per SM sub-partition: TMA issue throughput
-  // scales with the number of sub-partitions issuing); warp 8 forwards.
-  // fp8: warp 0 gathers the whole fp8 tile; the conversion warps convert it.
+  // bf16: each CTA gathers the chunks it reads into its own ring (score CTA: all
+  // 9, output CTA: the 8 latent chunks), so the score CTA refills a stage as soon
+  // as its QK^T is done with it, independently of the PV in the peer.  Warps 0,
+  // 6, 7 and 9 gather (one per SM sub-partition); warp w handles row groups
+  // g = w' + 4i (entries 4g..4g+3) and lane l < #chunks issues chunk l of each.
   if (!kFp8 && (warp == kWarpProducer || warp == kWarpConv0 || warp == kWarpConv0 + 1 ||
                 warp == kWarpConv0 + 3)) {
     const int pw = warp == kWarpProducer ? 0 : (warp == kWarpConv0 + 3 ? 3 : warp - kWarpConv0 + 1);
-    constexpr int npw = kFp8 ? 1 : 4;
-    const int nown = score_cta ? 5 : 4;                 // chunks this CTA gathers
+    const int c_mine = lane;    // chunk this lane gathers (lanes < nchunks)
     uint32_t kseq = 0;
+    const bool report = score_cta && pw == 0;
+    // Raw slot indices of tile j (lane holds entries lane and lane+32), -1 past the
+    // end; checked only when used, one iteration later, so the load is not waited on.
+    auto tile_idx = [&](const Item& it, int j, int32_t& x0, int32_t& x1) {
+      const int i0 = it.e0 + j * kBlockN + lane, i1 = i0 + 32;
+      x0 = i0 < it.e1 ? __ldg(p.kv_indices + it.kv_off + i0) : -1;
+      x1 = i1 < it.e1 ? __ldg(p.kv_indices + it.kv_off + i1) : -1;
+    };
+    // Invalid entries read row -1 (zero fill) and are reported once.
+    auto checked = [&](const Item& it, int j, int half, int32_t v) -> int32_t {
+      if (v >= 0 && v < p.num_slots) return v;
+      const int i = it.e0 + j * kBlockN + lane + 32 * half;
+      if (report && i < it.e1) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
+      return -1;
+    };
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
+      int32_t n0 = -1, n1 = -1;
+      if (nt > 0) tile_idx(it, 0, n0, n1);
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         const uint32_t ph = (kseq / kStages) & 1;
-        // 64 slot indices of this tile; invalid or past-the-end entries read row -1 (zero fill).
-        int32_t r0, r1;
-        {
-          const int i0 = it.e0 + j * kBlockN + lane, i1 = i0 + 32;
-          r0 = -1;
-          r1 = -1;
-          const bool report = score_cta && pw == 0;
-          if (i0 < it.e1) {
-            const int32_t s = __ldg(p.kv_indices + it.kv_off + i0);
-            if (s >= 0 && s < p.num_slots) r0 = s;
-            else if (report) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i0));
-          }
-          if (i1 < it.e1) {
-            const int32_t s = __ldg(p.kv_indices + it.kv_off + i1);
-            if (s >= 0 && s < p.num_slots) r1 = s;
-            else if (report) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i1));
-          }
-        }
+        // this tile's indices were loaded one iteration ago; start the next tile's now
+        const int32_t r0 = checked(it, j, 0, n0), r1 = checked(it, j, 1, n1);
+        if (j + 1 < nt) tile_idx(it, j + 1, n0, n1);
         if (!kFp8) {
+          // This warp's row groups g = pw + 4i (entries 4g..4g+3): their slot indices,
+          // taken from lanes (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8), before the wait.
+          int32_t a[4][4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int g = pw + 4 * i;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[i][e] = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, ((4 * g) & 31) + e);
+          }
           WAIT(&bars->empty[st], ph ^ 1, 1);
-          uint8_t* dst = tiles + st * kKTileBytes;
-          if (pw == 0 && lane == 0) {
-            // full: own direct chunk (score: RoPE) + the peer's forwarded half
-            mbar_arrive_expect_tx(&bars->full[st], (uint32_t)((score_cta ? 1 : 0) * kChunkBytes + 4 * kChunkBytes));
-            mbar_arrive_expect_tx(&bars->fwd[st], (uint32_t)(4 * kChunkBytes));
+          const uint32_t dst = smem_u32(tiles + st * kKTileBytes) + (uint32_t)(c_mine * kChunkBytes);
+          if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&bars->full[st], (uint32_t)(nchunks * kChunkBytes));
+          __syncwarp();
+          if (lane < nchunks) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              tma_gather4(dst + (uint32_t)((pw + 4 * i) * 512), &tmap_kv, c_mine * 64, a[i][0], a[i][1], a[i][2],
+                          a[i][3], &bars->full[st]);
           }
           __syncwarp();
-          for (int op = pw; op < nown * (kBlockN / 4); op += npw) {
-            const int k = op / (kBlockN / 4), g = op % (kBlockN / 4);
-            const int c = score_cta ? (k < 4 ? k : 8) : 4 + k;
-            // rows 4g..4g+3 live in lanes (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8)
-            const int src = (4 * g) & 31;
-            const int32_t a0 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src);
-            const int32_t a1 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 1);
-            const int32_t a2 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 2);
-            const int32_t a3 = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, src + 3);
-            if (lane == 0)
-              tma_gather4(smem_u32(dst + c * kChunkBytes + g * 512), &tmap_kv, c * 64, a0, a1, a2, a3,
-                          c == 8 ? &bars->full[st] : &bars->fwd[st]);
-          }
         }
       }
     }
@@ -287,32 +279,8 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   // ======================================================================= fp8: warp 0 has no job
   else if (warp == kWarpProducer) {
   }
-  // ======================================================================= bf16: forward half tiles
+  // ======================================================================= bf16: warp 8 has no job
   else if (!kFp8 && warp == kWarpConv0 + 2) {
-    uint32_t kseq = 0;
-    const uint32_t half_off = score_cta ? 0u : (uint32_t)(4 * kChunkBytes);
-    FOR_ITEMS(idx) {
-      const Item it = load_item(p, idx);
-      const int nt = item_tiles(it);
-      for (int j = 0; j < nt; ++j, ++kseq) {
-        const int st = kseq % kStages;
-        WAIT(&bars->fwd[st], (kseq / kStages) & 1, 5);
-        WAITC(&bars->pfree[st], ((kseq / kStages) & 1) ^ 1, 7);
-        if (lane == 0) {
-          const uint32_t src = smem_u32(tiles + st * kKTileBytes) + half_off;
-          const uint32_t peer = rank ^ 1u;
-          bulk_copy_to_peer(mapa(src, peer), src, 4 * kChunkBytes, mapa(smem_u32(&bars->full[st]), peer));
-          mbar_arrive(&bars->full[st]);
-        }
-        __syncwarp();
-      }
-    }
-    // The peer's last multicast commits target this CTA's barriers: they must
-    // land before this CTA exits.
-    for (int k = 0; k < kStages && (int)kseq - 1 - k >= 0; ++k) {
-      const uint32_t s2 = kseq - 1 - k;
-      WAITC(&bars->pfree[s2 % kStages], (s2 / kStages) & 1, 6);
-    }
   }
   // ======================================================================= fp8: load + convert
   // The four conversion warps read the indexed fp8 rows straight from global
@@ -325,21 +293,27 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     const int per = 16 * units / 32;                       // units per lane per tile
     const uint8_t* pool = static_cast<const uint8_t*>(p.kv);
     uint32_t kseq = 0;
+    // Raw slot index of entry 16cw + lane (lanes < 16) of tile j, -1 past the end;
+    // checked only when used, one iteration later, so the load is not waited on.
+    auto tile_slot = [&](const Item& it, int j) -> int32_t {
+      const int i = it.e0 + j * kBlockN + 16 * cw + lane;
+      return lane < 16 && i < it.e1 ? __ldg(p.kv_indices + it.kv_off + i) : -1;
+    };
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
+      int32_t nslot = nt > 0 ? tile_slot(it, 0) : -1;
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         const uint32_t ph = (kseq / kStages) & 1;
-        int32_t myslot = -1;
-        if (lane < 16) {
+        // this tile's index was loaded one iteration ago; start the next tile's now
+        int32_t myslot = nslot;
+        if (!(myslot >= 0 && myslot < p.num_slots)) {
           const int i = it.e0 + j * kBlockN + 16 * cw + lane;
-          if (i < it.e1) {
-            const int32_t sl = __ldg(p.kv_indices + it.kv_off + i);
-            if (sl >= 0 && sl < p.num_slots) myslot = sl;
-            else if (score_cta) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
-          }
+          if (score_cta && lane < 16 && i < it.e1) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
+          myslot = -1;
         }
+        if (j + 1 < nt) nslot = tile_slot(it, j + 1);
         uint4 raw[kDqk / 32];
 #pragma unroll
         for (int k = 0; k < kDqk / 32; ++k) {
@@ -396,13 +370,14 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         WAITC(&bars->full[st], (kseq / kStages) & 1, 12);
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t kbase = smem_u32(tiles + st * kKTileBytes);
-          for (int k = 0; k < kDqk / 16; ++k) {
-            const uint64_t bdesc = smem_desc_sw128(kbase + (k >> 2) * kChunkBytes + (k & 3) * 32, 16, 1024);
-            mma_ts(tmem + kTmemS + sb * kBlockN, tmem + kTmemQ + 8 * k, bdesc, idesc, k > 0);
-          }
+          // B descriptor of K step k: chunk k/4, 32-byte column offset k%4 (start address field is addr>>4)
+          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), 16, 1024);
+          const uint32_t dS = tmem + kTmemS + sb * kBlockN;
+#pragma unroll
+          for (int k = 0; k < kDqk / 16; ++k)
+            mma_ts(dS, tmem + kTmemQ + 8 * k, bdesc0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
+                   idesc, k > 0);
           mma_commit(&bars->empty[st]);
-          if (!kFp8) mma_commit_mc(&bars->pfree[st], 0x2);
           mma_commit(&bars->s_full[sb]);
         }
         __syncwarp();
@@ -431,17 +406,17 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         WAIT(&bars->corr_done[pb], pph, 23);
         fence_after_sync();
         if (lane == 0) {
-          const uint32_t vbase = smem_u32(tiles + st * kKTileBytes);
-          const uint32_t pbase = smem_u32(pbufs + pb * kPBufBytes);
+          const uint64_t adesc0 = smem_desc_sw128(smem_u32(pbufs + pb * kPBufBytes), 16, 1024);
+          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), kChunkBytes, 1024);
+#pragma unroll
           for (int h = 0; h < 2; ++h) {
-            for (int k = 0; k < kBlockN / 16; ++k) {
-              const uint64_t adesc = smem_desc_sw128(pbase + k * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(vbase + (4 * h) * kChunkBytes + k * 2048, kChunkBytes, 1024);
-              mma_ss(tmem + kTmemO + 256 * h, adesc, bdesc, idesc, (j > 0 || k > 0) ? 1u : 0u);
-            }
+#pragma unroll
+            for (int k = 0; k < kBlockN / 16; ++k)
+              mma_ss(tmem + kTmemO + 256 * h, adesc0 + (uint64_t)((k * 32) >> 4),
+                     bdesc0 + (uint64_t)(((4 * h) * kChunkBytes + k * 2048) >> 4), idesc,
+                     (j > 0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&bars->empty[st]);
-          if (!kFp8) mma_commit_mc(&bars->pfree[st], 0x1);
           mma_commit_mc(&bars->p_empty[pb], 0x1);
           mma_commit(&bars->o_ready[pb]);
         }
