@@ -42,16 +42,22 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 320;          // 10 warps
+// 12 warps for bf16 pools (seven of them gather), 10 for fp8 (warps 10-11 would
+// only slow the conversion warps down).
+constexpr int threads_for(bool fp8) { return fp8 ? 320 : 384; }
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpRow0 = 2;           // 4 row warps: softmax (rank 0) / correction+epilogue (rank 1)
-constexpr int kWarpConv0 = 6;          // 4 fp8 conversion warps
+constexpr int kWarpConv0 = 6;          // 4 fp8 conversion warps (bf16: KV gathers)
 constexpr int kStages = 2;             // KV tile ring
 constexpr int kPBufs = 2;              // P hand-off ring
 
 constexpr int kChunkBytes = kBlockN * 128;          // 64 entries x 64 bf16 columns = 8 KB
 constexpr int kKTileBytes = 9 * kChunkBytes;        // 576 columns (score CTA)
+// fp8: the tile's raw e4m3 rows are gathered into the upper half of the stage
+// (three 192-byte column blocks of [64 rows][192 B]) and converted in place.
+constexpr int kF8Off = kKTileBytes / 2;             // 36 KB
+constexpr int kF8BlockBytes = kBlockN * 192;        // 12 KB
 constexpr int kPBytes = kRows * 128;                // P: 128 rows x 64 bf16
 constexpr int kPStatsOff = kPBytes;                 // alpha[128], m[128], l[128], flags[4]
 constexpr int kPBufBytes = kPBytes + 3 * 512 + 512; // 18 KB, multiple of 16
@@ -72,6 +78,8 @@ constexpr uint32_t kTmemO = 0;       // output CTA: O, 512 columns
 struct Bars {
   uint64_t full[kStages];     // KV tile landed (TMA or fp8 conversion)
   uint64_t empty[kStages];    // KV tile consumed by this CTA's MMA
+  uint64_t full8[kStages];    // fp8: raw e4m3 rows of the tile landed (TMA)
+  uint64_t cv_sync;           // fp8: the conversion warps finished reading the raw rows
   uint64_t s_full[2];         // score CTA: S tile computed
   uint64_t s_free[2];         // score CTA: S tile read out
   uint64_t q_full;            // score CTA: Q written to TMEM
@@ -158,8 +166,28 @@ __device__ __forceinline__ void store_row32(const DecodeParams& p, float* dst_f3
   }
 }
 
+// 16 e4m3 values (unit u of 64-column chunk c of tile row `row`) -> two 16-byte
+// bf16 units of the swizzled tile.  Exact: the f16 bits from the hardware e4m3
+// conversion are placed in a bf16 word with the same exponent field, which
+// scales every value by 2^-112 (folded into the logit and output scales).
+__device__ __forceinline__ void fp8_unit_to_tile(uint8_t* stage, int row, int c, int u, const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h0, h1;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)(w[q] & 0xFFFF)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)(w[q] >> 16)));
+    o[2 * q] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
+    o[2 * q + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
+  }
+  uint8_t* base = stage + c * kChunkBytes;
+  *reinterpret_cast<uint4*>(base + swz(row, 2 * u)) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(base + swz(row, 2 * u + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1)
 mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
@@ -179,6 +207,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], kFp8 ? 4 : 1);
       mbar_init(&bars->empty[s], 1);
+      mbar_init(&bars->full8[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars->s_full[b], 1);
@@ -194,6 +223,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       mbar_init(&bars->o_ready[b], 1);
     }
     mbar_init(&bars->o_free, 4);
+    mbar_init(&bars->cv_sync, 4);
     mbar_init(&bars->mrg_a, 4);
     mbar_init(&bars->mrg_b, 1);
     mbar_init(&bars->mrg_c, 4);
@@ -212,18 +242,28 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
   const uint32_t tmem = bars->tmem_base;
   uint8_t* tiles = smem + kOffTiles;
   uint8_t* pbufs = smem + kOffPBuf;
-  const int nchunks = score_cta ? 9 : 8;
 
   // ======================================================================= producer
-  // bf16: each CTA gathers the chunks it reads into its own ring (score CTA: all
-  // 9, output CTA: the 8 latent chunks), so the score CTA refills a stage as soon
-  // as its QK^T is done with it, independently of the PV in the peer.  Warps 0,
-  // 6, 7 and 9 gather (one per SM sub-partition); warp w handles row groups
-  // g = w' + 4i (entries 4g..4g+3) and lane l < #chunks issues chunk l of each.
-  if (!kFp8 && (warp == kWarpProducer || warp == kWarpConv0 || warp == kWarpConv0 + 1 ||
-                warp == kWarpConv0 + 3)) {
-    const int pw = warp == kWarpProducer ? 0 : (warp == kWarpConv0 + 3 ? 3 : warp - kWarpConv0 + 1);
-    const int c_mine = lane;    // chunk this lane gathers (lanes < nchunks)
+  // KV gathers with TMA.  One gather op moves 4 rows (entries 4g..4g+3, row
+  // group g) x one column block; a tile needs 16 groups x nblk blocks.  Issue
+  // cost is mostly per warp instruction, so each lane owns one op and a warp
+  // issues its share of the tile in one instruction (two for fp8).
+  //   bf16: each CTA gathers the 64-column chunks it reads into its own ring
+  //   (score CTA: all 9, output CTA: the 8 latent chunks), so the score CTA
+  //   refills a stage as soon as its QK^T is done with it; warps 0 and 6-11 share
+  //   the 144 (128) ops.
+  //   fp8: the raw e4m3 rows, three 192-byte column blocks per row, land in the
+  //   stage's upper half for the conversion warps; warp 0 issues the 48 ops
+  //   alone (more issuing warps slowed the conversion warps beside them).
+  if (warp == kWarpProducer || (!kFp8 && warp >= kWarpConv0)) {
+    constexpr int npw = kFp8 ? 1 : 7;
+    constexpr int kOpsPerLane = kFp8 ? 2 : 1;
+    const int pw = warp == kWarpProducer ? 0 : warp - kWarpConv0 + 1;
+    const int nblk = kFp8 ? 3 : (score_cta ? 9 : 8);
+    const int nops = 16 * nblk;
+    const int per = (nops + npw - 1) / npw;             // ops of this warp: [o_begin, o_end)
+    const int o_begin = pw * per, o_end = o_begin + per < nops ? o_begin + per : nops;
+    const uint32_t tx = (uint32_t)(16 * nblk * (kFp8 ? 4 * 192 : 512));
     uint32_t kseq = 0;
     const bool report = score_cta && pw == 0;
     // Raw slot indices of tile j (lane holds entries lane and lane+32), -1 past the
@@ -251,101 +291,84 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         // this tile's indices were loaded one iteration ago; start the next tile's now
         const int32_t r0 = checked(it, j, 0, n0), r1 = checked(it, j, 1, n1);
         if (j + 1 < nt) tile_idx(it, j + 1, n0, n1);
-        if (!kFp8) {
-          // This warp's row groups g = pw + 4i (entries 4g..4g+3): their slot indices,
-          // taken from lanes (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8), before the wait.
-          int32_t a[4][4];
+        // slot indices of the group of each of this lane's ops, from lanes
+        // (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8), before the wait
+        int32_t a[kOpsPerLane][4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int g = pw + 4 * i;
+        for (int q = 0; q < kOpsPerLane; ++q) {
+          const int g = ((o_begin + 32 * q + lane) / nblk) & 15;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) a[i][e] = __shfl_sync(0xffffffffu, g < 8 ? r0 : r1, ((4 * g) & 31) + e);
+          for (int e = 0; e < 4; ++e) {
+            const int32_t x0 = __shfl_sync(0xffffffffu, r0, ((4 * g) & 31) + e);
+            const int32_t x1 = __shfl_sync(0xffffffffu, r1, ((4 * g) & 31) + e);
+            a[q][e] = g < 8 ? x0 : x1;
           }
-          WAIT(&bars->empty[st], ph ^ 1, 1);
-          const uint32_t dst = smem_u32(tiles + st * kKTileBytes) + (uint32_t)(c_mine * kChunkBytes);
-          if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&bars->full[st], (uint32_t)(nchunks * kChunkBytes));
-          __syncwarp();
-          if (lane < nchunks) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              tma_gather4(dst + (uint32_t)((pw + 4 * i) * 512), &tmap_kv, c_mine * 64, a[i][0], a[i][1], a[i][2],
-                          a[i][3], &bars->full[st]);
-          }
-          __syncwarp();
         }
+        WAIT(&bars->empty[st], ph ^ 1, 1);
+        uint64_t* bar = kFp8 ? &bars->full8[st] : &bars->full[st];
+        if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar, tx);
+        __syncwarp();
+        const uint32_t base = smem_u32(tiles + st * kKTileBytes);
+#pragma unroll
+        for (int q = 0; q < kOpsPerLane; ++q) {
+          const int o = o_begin + 32 * q + lane;
+          if (o < o_end) {
+            const int g = o / nblk, c = o - g * nblk;
+            if (kFp8)
+              tma_gather4(base + (uint32_t)(kF8Off + c * kF8BlockBytes + g * 4 * 192), &tmap_kv, 192 * c, a[q][0],
+                          a[q][1], a[q][2], a[q][3], bar);
+            else
+              tma_gather4(base + (uint32_t)(c * kChunkBytes + g * 512), &tmap_kv, c * 64, a[q][0], a[q][1], a[q][2],
+                          a[q][3], bar);
+          }
+        }
+        __syncwarp();
       }
     }
   }
-  // ======================================================================= fp8: warp 0 has no job
-  else if (warp == kWarpProducer) {
-  }
-  // ======================================================================= bf16: warp 8 has no job
-  else if (!kFp8 && warp == kWarpConv0 + 2) {
-  }
-  // ======================================================================= fp8: load + convert
-  // The four conversion warps read the indexed fp8 rows straight from global
-  // memory (16-byte loads, all issued before waiting for the stage), convert
-  // them in registers and write the swizzled bf16 tile.  Warp cw owns rows
-  // 16cw .. 16cw+15 of every tile.
+  // ======================================================================= fp8: convert in place
+  // The four conversion warps turn the tile's raw e4m3 rows (gathered by warp 0
+  // into the stage's upper half) into the swizzled bf16 tile.  Warp cw owns rows
+  // 16cw .. 16cw+15.  Chunks 0-3 are written first (below the raw rows); the raw
+  // bytes of chunks 4.. are read into registers, and once all four warps hold
+  // theirs the remaining chunks overwrite the raw area.
   else if (kFp8 && warp >= kWarpConv0) {
     const int cw = warp - kWarpConv0;
-    const int units = score_cta ? kDqk / 16 : kDv / 16;   // 16-byte fp8 units per row
-    const int per = 16 * units / 32;                       // units per lane per tile
-    const uint8_t* pool = static_cast<const uint8_t*>(p.kv);
-    uint32_t kseq = 0;
-    // Raw slot index of entry 16cw + lane (lanes < 16) of tile j, -1 past the end;
-    // checked only when used, one iteration later, so the load is not waited on.
-    auto tile_slot = [&](const Item& it, int j) -> int32_t {
-      const int i = it.e0 + j * kBlockN + 16 * cw + lane;
-      return lane < 16 && i < it.e1 ? __ldg(p.kv_indices + it.kv_off + i) : -1;
-    };
+    uint32_t kseq = 0, cv_ph = 0;
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
-      int32_t nslot = nt > 0 ? tile_slot(it, 0) : -1;
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
-        const uint32_t ph = (kseq / kStages) & 1;
-        // this tile's index was loaded one iteration ago; start the next tile's now
-        int32_t myslot = nslot;
-        if (!(myslot >= 0 && myslot < p.num_slots)) {
-          const int i = it.e0 + j * kBlockN + 16 * cw + lane;
-          if (score_cta && lane < 16 && i < it.e1) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
-          myslot = -1;
-        }
-        if (j + 1 < nt) nslot = tile_slot(it, j + 1);
-        uint4 raw[kDqk / 32];
+        WAIT(&bars->full8[st], (kseq / kStages) & 1, 4);
+        uint8_t* stage = tiles + st * kKTileBytes;
+        const uint8_t* raw = stage + kF8Off;
+        // chunks 0-3: 16 rows x 4 chunks x 4 units of 16 fp8 values, 8 per lane
 #pragma unroll
-        for (int k = 0; k < kDqk / 32; ++k) {
-          raw[k] = make_uint4(0, 0, 0, 0);
-          if (k < per) {
-            const int flat = k * 32 + lane, e = flat / units, u = flat % units;
-            const int32_t sl = __shfl_sync(0xffffffffu, myslot, e);
-            if (sl >= 0) raw[k] = __ldg(reinterpret_cast<const uint4*>(pool + (int64_t)sl * kDqk + u * 16));
+        for (int k = 0; k < 8; ++k) {
+          const int f = k * 32 + lane, row = 16 * cw + (f >> 4), c = (f >> 2) & 3, u = f & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(raw + (c / 3) * kF8BlockBytes + row * 192 + (c % 3) * 64 + u * 16);
+          fp8_unit_to_tile(stage, row, c, u, v);
+        }
+        // chunks 4.. (score: 4-8, output: 4-7) into registers
+        uint4 rb[10];
+        const int nb = score_cta ? 5 : 4;
+#pragma unroll
+        for (int k = 0; k < 10; ++k) {
+          if (k < 2 * nb) {
+            const int f = k * 32 + lane, row = 16 * cw + f / (4 * nb), c = 4 + (f % (4 * nb)) / 4, u = f & 3;
+            rb[k] = *reinterpret_cast<const uint4*>(raw + (c / 3) * kF8BlockBytes + row * 192 + (c % 3) * 64 + u * 16);
           }
         }
-        WAIT(&bars->empty[st], ph ^ 1, 4);
-        uint8_t* dst = tiles + st * kKTileBytes;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->cv_sync);
+        WAIT(&bars->cv_sync, cv_ph, 5);
+        cv_ph ^= 1;
 #pragma unroll
-        for (int k = 0; k < kDqk / 32; ++k) {
-          if (k < per) {
-            const int flat = k * 32 + lane, e = 16 * cw + flat / units, u = flat % units;
-            const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-            uint32_t o[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t h0, h1;
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h0) : "h"((uint16_t)(w[q] & 0xFFFF)));
-              asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h1) : "h"((uint16_t)(w[q] >> 16)));
-              // f16 bits -> bf16 bits with the same exponent field: value * 2^-112, exact
-              o[2 * q] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
-              o[2 * q + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
-            }
-            // 16 values = two 16-byte units of 64-column chunk u/4
-            uint8_t* base = dst + (u >> 2) * kChunkBytes;
-            const int u0 = (u & 3) * 2;
-            *reinterpret_cast<uint4*>(base + swz(e, u0)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(base + swz(e, u0 + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+        for (int k = 0; k < 10; ++k) {
+          if (k < 2 * nb) {
+            const int f = k * 32 + lane, row = 16 * cw + f / (4 * nb), c = 4 + (f % (4 * nb)) / 4, u = f & 3;
+            fp8_unit_to_tile(stage, row, c, u, rb[k]);
           }
         }
         fence_proxy_async_smem();
@@ -367,12 +390,13 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       for (int j = 0; j < nt; ++j, ++kseq, ++sseq) {
         const int st = kseq % kStages, sb = sseq & 1;
         WAIT(&bars->s_free[sb], ((sseq >> 1) & 1) ^ 1, 11);
-        WAITC(&bars->full[st], (kseq / kStages) & 1, 12);
+        const uint32_t kph = (kseq / kStages) & 1;
+        // B descriptor of K step k: chunk k/4, 32-byte column offset k%4 (start address field is addr>>4)
+        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), 16, 1024);
+        const uint32_t dS = tmem + kTmemS + sb * kBlockN;
+        WAITC(&bars->full[st], kph, 12);
         fence_after_sync();
         if (lane == 0) {
-          // B descriptor of K step k: chunk k/4, 32-byte column offset k%4 (start address field is addr>>4)
-          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), 16, 1024);
-          const uint32_t dS = tmem + kTmemS + sb * kBlockN;
 #pragma unroll
           for (int k = 0; k < kDqk / 16; ++k)
             mma_ts(dS, tmem + kTmemQ + 8 * k, bdesc0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
@@ -783,7 +807,7 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
       return MLA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_for(kFp8), 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -805,7 +829,7 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
     kp.scale_log2 = dp.scale_log2 * 5.192296858534828e33f;
     kp.out_scale = dp.out_scale * 5.192296858534828e33f;
   }
-  kern<<<2 * clusters, kThreads, smem, (cudaStream_t)stream>>>(tmap, kp);
+  kern<<<2 * clusters, threads_for(kFp8), smem, (cudaStream_t)stream>>>(tmap, kp);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
