@@ -45,8 +45,8 @@ def build_workload(name: str):
     if name == "draft_block_bf16":
         return mi.draft_block_bf16(), dict(mode=0, cap=8192, shards=None)
     if name == "verify_fp8":
-        w = mi.verify_fp8()
-        return w, dict(mode=0, cap=w.meta["kv_len_cap"], shards=None)
+        # the host split plan, built from the real kv_indptr
+        return mi.verify_fp8(), dict(mode=2, cap=0, shards=None)
     if name == "long_skewed_fp8":
         return mi.long_skewed_fp8(), dict(mode=1, cap=0, shards=None)
     if name == "cp_shards_bf16":
@@ -306,6 +306,8 @@ def main():
                             kv_len_cap=extra["cap"])
     if extra["mode"] == m.MLA_PLAN_STATIC:
         runner.set_host_plan(None, w.qo_indptr)
+    elif extra["mode"] == m.MLA_PLAN_HOST:
+        runner.set_host_plan(w.kv_indptr, w.qo_indptr)
     dev = mi.to_device(w)
     out_fp32 = shards is not None
     o = torch.empty(w.total_q, w.num_heads, 512, device="cuda",
@@ -359,6 +361,12 @@ def main():
     o_h = torch.empty_like(out_final[0], device="cpu").pin_memory()
     l_h = torch.empty_like(out_final[1], device="cpu").pin_memory()
     h2d = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in idx_h.values())
+    # a HOST plan follows the step's lengths: built on the host and uploaded every step
+    host_plan = extra["mode"] == m.MLA_PLAN_HOST
+    if host_plan:
+        kvp_np, qop_np = w.kv_indptr.copy(), w.qo_indptr.copy()
+        plan_h = torch.empty_like(runner.plan_d, device="cpu").pin_memory()
+        h2d += plan_h.numel() * 4
     d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
@@ -368,6 +376,11 @@ def main():
         dev["q"].copy_(q_h, non_blocking=True)
         for k, t in idx_h.items():
             dev[k].copy_(t, non_blocking=True)
+        if host_plan:
+            # (every step rebuilds the same bytes, so refilling the pinned buffer
+            # while the previous step's copy may still be queued is harmless)
+            plan_h.numpy()[:] = m.mla_decode_plan(runner.params, kvp_np, qop_np)
+            runner.plan_d.copy_(plan_h, non_blocking=True)
         step()
         o_h.copy_(out_final[0], non_blocking=True)
         l_h.copy_(out_final[1], non_blocking=True)
@@ -393,7 +406,7 @@ def main():
             "data": "synthetic",
             "config": {"workload": args.config, "batch": w.batch, "heads": w.num_heads,
                        "q_len": int(w.q_lens().max()), "kv_tokens": int(w.kv_indptr[-1]),
-                       "kv_dtype": w.kv_dtype, "causal": w.causal, "plan": "static" if extra["mode"] == 0 else "dynamic",
+                       "kv_dtype": w.kv_dtype, "causal": w.causal, "plan": ("static", "dynamic", "host")[extra["mode"]],
                        "algo": args.algo, "workers": workers, "l2": "flushed (256 MB write) between timed steps"},
             "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],

@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 1
+#define MLA_ABI_VERSION 2
 #define MLA_D_QK 576             /* latent 512 + RoPE 64 */
 #define MLA_D_V 512
 #define MLA_ROWS_PER_GROUP 128   /* query rows (t,h) handled together */
@@ -87,7 +87,19 @@ typedef enum {
 
 typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1 } mla_kv_dtype;
 typedef enum { MLA_OUT_BF16 = 0, MLA_OUT_FP32 = 1 } mla_out_dtype;
-typedef enum { MLA_PLAN_STATIC = 0, MLA_PLAN_DYNAMIC = 1 } mla_plan_mode;
+/* Plan modes.
+ *   STATIC   built on the host from the query-row counts and a KV capacity
+ *            (kv_len_cap) only: one plan serves every call of that shape, so a
+ *            captured CUDA graph can replay with any lengths.
+ *   DYNAMIC  rebuilt on the device by every mla_decode_fwd from the real
+ *            lengths (the persistent-kernel re-plan).
+ *   HOST     built on the host by mla_decode_plan from the real kv_indptr and
+ *            uploaded by the caller; mla_decode_fwd uses it as is.  Splits and
+ *            item order are sized for those lengths.
+ * In every mode the forward takes each split's KV range from the lengths it is
+ * called with, so a plan never gives a wrong result for other lengths, only a
+ * less balanced one. */
+typedef enum { MLA_PLAN_STATIC = 0, MLA_PLAN_DYNAMIC = 1, MLA_PLAN_HOST = 2 } mla_plan_mode;
 
 /* Kernel family.  MLA_ALGO_TENSOR (default) is the tcgen05/TMEM kernel;
  * MLA_ALGO_CUDA_CORE is a plain CUDA-core kernel of the same operation, kept for

@@ -17,7 +17,7 @@ The constants and the tie-break rules below are this build's choices.
 Specification (all integers, 64-bit intermediates):
   For request b:  T_b = qo_indptr[b+1]-qo_indptr[b],  L_b = kv_indptr[b+1]-kv_indptr[b]
     G_b = ceil(H*T_b / ROWS)          query-row groups (0 when T_b = 0)
-    N_b = ceil(L_b / BLOCK_N)         DYNAMIC: from the real length
+    N_b = ceil(L_b / BLOCK_N)         DYNAMIC, HOST: from the real length
           ceil(cap / BLOCK_N)         STATIC: from the capacity kv_len_cap
   total  = sum_b G_b * N_b
   target = max(MIN_TILES, ceil(total / W))             W = num_workers
@@ -54,6 +54,7 @@ MIN_TILES = 4
 COST_CLAMP = 65535
 STATIC = 0
 DYNAMIC = 1
+HOST = 2            # built on the host from the real lengths, used as is
 HEADER_INTS = 16
 
 
@@ -73,14 +74,14 @@ def plan_ints(batch: int, num_heads: int, max_q_len: int, num_workers: int) -> i
 def build_plan(batch: int, num_heads: int, max_q_len: int, num_workers: int, kv_len_cap: int,
                mode: int, kv_indptr: Optional[np.ndarray], qo_indptr: np.ndarray) -> np.ndarray:
     """Return the plan buffer as an int32 array (raises ValueError on invalid input)."""
-    if batch < 0 or num_heads < 1 or max_q_len < 0 or num_workers < 1 or mode not in (STATIC, DYNAMIC):
+    if batch < 0 or num_heads < 1 or max_q_len < 0 or num_workers < 1 or mode not in (STATIC, DYNAMIC, HOST):
         raise ValueError("invalid plan parameters")
     if mode == STATIC and kv_len_cap < 0:
         raise ValueError("negative kv_len_cap")
     T = [int(qo_indptr[b + 1]) - int(qo_indptr[b]) for b in range(batch)]
     if any(t < 0 or t > max_q_len for t in T):
         raise ValueError("q length outside [0, max_q_len]")
-    if mode == DYNAMIC:
+    if mode in (DYNAMIC, HOST):
         L = [int(kv_indptr[b + 1]) - int(kv_indptr[b]) for b in range(batch)]
         if any(x < 0 for x in L):
             raise ValueError("decreasing kv_indptr")

@@ -23,6 +23,8 @@ def run(w: mi.Workload, *, algo: int, mode: int = 1, num_workers=None, kv_len_ca
                                 kv_len_cap=kv_len_cap)
         if mode == m.MLA_PLAN_STATIC:
             runner.set_host_plan(None, w.qo_indptr)
+        elif mode == m.MLA_PLAN_HOST:
+            runner.set_host_plan(w.kv_indptr, w.qo_indptr)
     if o is None:
         o = torch.full((w.total_q, H, 512), float("nan"), device="cuda",
                        dtype=torch.float32 if out_fp32 else torch.bfloat16)

@@ -58,7 +58,7 @@ def test_host_plan_matches_spec_random(seed):
     H = int(rng.choice([1, 3, 16, 64, 96, 128]))
     maxT = int(rng.integers(0, 9))
     W = int(rng.integers(1, 400))
-    mode = int(rng.integers(0, 2))
+    mode = int(rng.integers(0, 3))
     T = rng.integers(0, maxT + 1, size=B)
     L = np.floor(np.exp(rng.uniform(0, np.log(300000), size=B))).astype(np.int64)
     L[rng.random(B) < 0.15] = 0
@@ -78,7 +78,7 @@ def test_host_plan_for_the_five_workloads():
     shapes.append((128, 96, 8, [4096] * 128, [8] * 128))
     for B, H, maxT, L, T in shapes:
         for W in (1, 76, 152, 608):
-            for mode in (po.STATIC, po.DYNAMIC):
+            for mode in (po.STATIC, po.DYNAMIC, po.HOST):
                 kvp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
                 qop = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
                 _host_vs_oracle(B, H, maxT, W, 16384, mode, kvp, qop)
@@ -105,6 +105,23 @@ def test_host_plan_rejects_bad_input():
                           np.array([0, 5, 9]), np.array([0, 1, 2]))
     with pytest.raises(m.MlaError):
         m.mla_decode_plan_size(m.plan_params(1, 16, 1, 0, 0, m.MLA_PLAN_DYNAMIC))
+    with pytest.raises(m.MlaError):   # a HOST plan is built from the real lengths
+        m.mla_decode_plan(m.plan_params(2, 16, 1, 4, 0, m.MLA_PLAN_HOST), None, np.array([0, 1, 2]))
+    with pytest.raises(m.MlaError):   # no such mode
+        m.mla_decode_plan(m.plan_params(2, 16, 1, 4, 0, 3), np.array([0, 5, 9]), np.array([0, 1, 2]))
+
+
+def test_host_mode_plan_is_the_real_length_plan():
+    """HOST and DYNAMIC plans are the same plan from the same lengths (only the
+    header's mode word differs); a STATIC plan ignores the lengths."""
+    rng = np.random.default_rng(5)
+    L = rng.integers(1, 20000, size=24)
+    kvp = np.concatenate([[0], np.cumsum(L)]).astype(np.int32)
+    qop = np.arange(0, 25 * 4, 4, dtype=np.int32)[:25]
+    host = m.mla_decode_plan(m.plan_params(24, 128, 4, 76, 0, m.MLA_PLAN_HOST), kvp, qop)
+    dyn = m.mla_decode_plan(m.plan_params(24, 128, 4, 76, 0, m.MLA_PLAN_DYNAMIC), kvp, qop)
+    diff = np.nonzero(host != dyn)[0]
+    assert list(diff) == [6] and host[6] == m.MLA_PLAN_HOST and dyn[6] == m.MLA_PLAN_DYNAMIC
 
 
 def test_fwd_rejects_bad_arguments_before_touching_the_device():

@@ -72,7 +72,7 @@ def test_draft_block_equals_flattened_rows(algo):
     hz.assert_close(O2, L2, Oref, Lref, "bf16")
 
 
-@pytest.mark.parametrize("mode", [0, 1], ids=["static", "dynamic"])
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["static", "dynamic", "host"])
 def test_verify_fp8_small(algo, mode):
     w = mi.verify_fp8(scale=1 / 16)
     _check(w, algo, mode=mode, kv_len_cap=w.meta["kv_len_cap"], num_workers=608)
@@ -82,6 +82,26 @@ def test_verify_fp8_full_sampled_static(algo):
     w = mi.verify_fp8()
     _check(w, algo, mode=0, reqs=hz.sample_requests(w, 3), kv_len_cap=w.meta["kv_len_cap"],
            num_workers=608)
+
+
+def test_verify_fp8_full_sampled_host_plan(algo):
+    """The host plan built from the real kv_indptr (the plan the benchmark uses)."""
+    w = mi.verify_fp8()
+    _check(w, algo, mode=2, reqs=hz.sample_requests(w, 3, seed=11), num_workers=76)
+
+
+def test_host_plan_stays_correct_for_other_lengths():
+    """A HOST plan sized for one set of lengths, called with other lengths: the
+    split ranges follow the call's lengths, so the result is still exact."""
+    import token_mla_paged_gb300 as m
+    w0 = mi.verify_fp8(scale=1 / 16, seed=3)
+    w1 = mi.verify_fp8(scale=1 / 16, seed=4)
+    runner = m.DecodeRunner(w1.batch, w1.num_heads, 8, mode=m.MLA_PLAN_HOST, num_workers=76)
+    runner.set_host_plan(w0.kv_indptr, w0.qo_indptr)
+    O, L, _ = hz.run(w1, algo=m.MLA_ALGO_TENSOR, runner=runner)
+    assert hz.device_error(runner) == (0, 0)
+    Oref, Lref = mo.mla_decode_workload(w1)
+    hz.assert_close(O, L, Oref, Lref, "fp8")
 
 
 def test_long_skewed_fp8_small(algo):

@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
 MLA_OK = 0
 MLA_KV_BF16, MLA_KV_FP8_E4M3 = 0, 1
 MLA_OUT_BF16, MLA_OUT_FP32 = 0, 1
-MLA_PLAN_STATIC, MLA_PLAN_DYNAMIC = 0, 1
+MLA_PLAN_STATIC, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST = 0, 1, 2
 MLA_ALGO_TENSOR, MLA_ALGO_CUDA_CORE = 0, 1
 D_QK, D_V = 576, 512
 

@@ -16,7 +16,7 @@ namespace {
 bool params_valid(const mla_plan_params* p) {
   if (!p) return false;
   if (p->batch < 0 || p->num_heads < 1 || p->max_q_len < 0 || p->num_workers < 1) return false;
-  if (p->mode != MLA_PLAN_STATIC && p->mode != MLA_PLAN_DYNAMIC) return false;
+  if (p->mode != MLA_PLAN_STATIC && p->mode != MLA_PLAN_DYNAMIC && p->mode != MLA_PLAN_HOST) return false;
   if (p->mode == MLA_PLAN_STATIC && p->kv_len_cap < 0) return false;
   return true;
 }

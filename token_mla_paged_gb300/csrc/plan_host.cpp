@@ -4,11 +4,12 @@
 // that no forward call writes a plan and every CUDA graph reads constant memory
 // ("[DSV4] Tuned ASM FP8 decode with split plans; HCA on aiter's persistent
 // V4-NM kernel", Summary part 1).  In STATIC mode the plan depends only on the
-// query-row counts and a KV capacity; in DYNAMIC mode on the real KV lengths
-// (the same plan the device planner rebuilds at every call, Summary part 2).
+// query-row counts and a KV capacity; in DYNAMIC and HOST mode on the real KV
+// lengths (DYNAMIC: the same plan the device planner rebuilds at every call,
+// Summary part 2; HOST: built here from the CSR and used as is).
 //
 // Rules (integers only, 64-bit intermediates):
-//   G_b = ceil(H*T_b/128) row groups; N_b = ceil(L_b/64) tiles (DYNAMIC) or
+//   G_b = ceil(H*T_b/128) row groups; N_b = ceil(L_b/64) tiles (DYNAMIC, HOST) or
 //   ceil(cap/64) (STATIC); target = max(4, ceil(sum G_b*N_b / W));
 //   S_b = clamp(ceil(N_b/target), 1, 16); one item per (b, split s, group g),
 //   enumerated b-major, then s, then g; items sorted by min(cost, 65535)
@@ -24,11 +25,12 @@ namespace mla {
 mla_status plan_build_host(const mla_plan_params& p, const int32_t* kv_indptr,
                            const int32_t* qo_indptr, int32_t* out) {
   if (p.batch < 0 || p.num_heads < 1 || p.max_q_len < 0 || p.num_workers < 1 ||
-      (p.mode != MLA_PLAN_STATIC && p.mode != MLA_PLAN_DYNAMIC))
+      (p.mode != MLA_PLAN_STATIC && p.mode != MLA_PLAN_DYNAMIC && p.mode != MLA_PLAN_HOST))
     return MLA_ERR_INVALID_ARG;
   if (p.mode == MLA_PLAN_STATIC && p.kv_len_cap < 0) return MLA_ERR_INVALID_ARG;
   if (p.batch > 0 && qo_indptr == nullptr) return MLA_ERR_INVALID_ARG;
-  if (p.mode == MLA_PLAN_DYNAMIC && p.batch > 0 && kv_indptr == nullptr) return MLA_ERR_INVALID_ARG;
+  const bool real_lengths = p.mode != MLA_PLAN_STATIC;
+  if (real_lengths && p.batch > 0 && kv_indptr == nullptr) return MLA_ERR_INVALID_ARG;
 
   const PlanGeom geom = plan_geom(p);
   if (geom.items_cap > kCostClamp) return MLA_ERR_UNSUPPORTED;
@@ -39,7 +41,7 @@ mla_status plan_build_host(const mla_plan_params& p, const int32_t* kv_indptr,
     const int64_t T = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
     if (T < 0 || T > p.max_q_len) return MLA_ERR_INVALID_ARG;
     int64_t L;
-    if (p.mode == MLA_PLAN_DYNAMIC) {
+    if (real_lengths) {
       L = (int64_t)kv_indptr[b + 1] - kv_indptr[b];
       if (L < 0) return MLA_ERR_INVALID_ARG;
     } else {

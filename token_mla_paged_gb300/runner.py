@@ -6,7 +6,7 @@ from typing import Optional
 
 import numpy as np
 
-from . import (MLA_ALGO_TENSOR, MLA_PLAN_DYNAMIC, MLA_PLAN_STATIC, mla_decode_fwd,
+from . import (MLA_ALGO_TENSOR, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST, MLA_PLAN_STATIC, mla_decode_fwd,
                mla_decode_plan, mla_decode_plan_size, plan_params)
 
 
@@ -18,8 +18,10 @@ def default_workers(device=None) -> int:
 class DecodeRunner:
     """Owns one plan buffer and one workspace sized for `params`.
 
-    STATIC mode: call ``set_host_plan`` once (outside any graph) with host copies
-    of kv_indptr / qo_indptr; the plan is uploaded and then only read.
+    STATIC mode: call ``set_host_plan`` once (outside any graph) with the host
+    qo_indptr (kv_indptr unused); the plan is uploaded and then only read.
+    HOST mode: call ``set_host_plan`` with host copies of kv_indptr / qo_indptr
+    whenever the lengths change; the plan is built from the real lengths.
     DYNAMIC mode: every ``forward`` re-plans on the device.
     """
 
@@ -37,7 +39,7 @@ class DecodeRunner:
 
     def set_host_plan(self, kv_indptr_h: Optional[np.ndarray], qo_indptr_h: np.ndarray) -> np.ndarray:
         import torch
-        assert self.params.mode == MLA_PLAN_STATIC
+        assert self.params.mode in (MLA_PLAN_STATIC, MLA_PLAN_HOST)
         plan = mla_decode_plan(self.params, kv_indptr_h, qo_indptr_h)
         self.plan_d.copy_(torch.from_numpy(plan))
         self.host_plan = plan
