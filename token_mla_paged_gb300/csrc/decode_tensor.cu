@@ -67,7 +67,8 @@ constexpr int kOffBars = 0;
 constexpr int kOffData = 2048;
 constexpr int kOffTiles = kOffData;                                   // kStages x 72 KB
 constexpr int kOffPBuf = kOffTiles + kStages * kKTileBytes;           // kPBufs x 18 KB
-constexpr int kSmemBytes = kOffPBuf + kPBufs * kPBufBytes;
+constexpr int kOffEpi = kOffPBuf + kPBufs * kPBufBytes;              // output CTA: 4 x 4 KB epilogue staging
+constexpr int kSmemBytes = kOffEpi + 4 * 4096;
 constexpr int kSmemAlign = 1024;
 
 // TMEM columns.
@@ -93,11 +94,10 @@ struct Bars {
   uint64_t mrg_a;             // output CTA: the 4 row warps fenced their partial rows
   uint64_t mrg_b;             // output CTA: leader published the last-arriver verdict
   uint64_t mrg_c;             // output CTA: per-row merge weights ready
+  uint64_t mrg_d;             // output CTA: the 4 row warps are done with the weights
   uint32_t tmem_base;
   int abort;
   int merge_last;
-  float merge_m[kRows];
-  float merge_inv[kRows];
 };
 static_assert(sizeof(Bars) <= kOffData, "barrier block too large");
 
@@ -145,27 +145,6 @@ __device__ __forceinline__ int item_tiles(const Item& it) {
   return it.ok && it.e1 > it.e0 ? (it.e1 - it.e0 + kBlockN - 1) / kBlockN : 0;
 }
 
-// Store 32 consecutive output columns of one row (bf16 or fp32).
-__device__ __forceinline__ void store_row32(const DecodeParams& p, float* dst_f32, int64_t row, int c0,
-                                            const float (&v)[32]) {
-  if (dst_f32 != nullptr) {
-    float4* d = reinterpret_cast<float4*>(dst_f32 + c0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) d[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  } else {
-    uint4* d = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row * kDv + c0);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint4 u;
-      u.x = pack_bf16x2(v[8 * k + 0], v[8 * k + 1]);
-      u.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
-      u.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
-      u.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
-      d[k] = u;
-    }
-  }
-}
-
 // 16 e4m3 values (unit u of 64-column chunk c of tile row `row`) -> two 16-byte
 // bf16 units of the swizzled tile.  Exact: the f16 bits from the hardware e4m3
 // conversion are placed in a bf16 word with the same exponent field, which
@@ -184,6 +163,34 @@ __device__ __forceinline__ void fp8_unit_to_tile(uint8_t* stage, int row, int c,
   uint8_t* base = stage + c * kChunkBytes;
   *reinterpret_cast<uint4*>(base + swz(row, 2 * u)) = make_uint4(o[0], o[1], o[2], o[3]);
   *reinterpret_cast<uint4*>(base + swz(row, 2 * u + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Epilogue write-back of one 32-column block of a warp's 32 rows, staged at stg
+// (128-byte row pitch, 16-byte unit k of row r at unit k ^ (r & 7)): each store
+// instruction writes whole row segments, 128 bytes (fp32) or 64 bytes (bf16).
+template <bool kF32>
+__device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q4, int c, const Item& it,
+                                             const DecodeParams& p) {
+  constexpr int kUsh = kF32 ? 3 : 2;          // log2 of 16-byte units per row segment
+  constexpr int kN = 1 << kUsh;
+  uint4 val[kN];
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int rl = (i << (5 - kUsh)) + (lane >> kUsh), u = lane & (kN - 1);
+    val[i] = *reinterpret_cast<const uint4*>(stg + rl * 128 + ((u ^ (rl & 7)) << 4));
+  }
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    const int rl = (i << (5 - kUsh)) + (lane >> kUsh), u = lane & (kN - 1);
+    const int ri = 32 * q4 + rl;               // row within the item
+    if (ri < it.nrows) {
+      void* dst;
+      if (!kF32) dst = static_cast<__nv_bfloat16*>(p.o) + (it.q_row_base + it.row0 + ri) * kDv + 32 * c + 8 * u;
+      else if (it.slot >= 0) dst = p.part_o + ((int64_t)it.slot * kRows + ri) * kDv + 32 * c + 4 * u;
+      else dst = static_cast<float*>(p.o) + (it.q_row_base + it.row0 + ri) * kDv + 32 * c + 4 * u;
+      *reinterpret_cast<uint4*>(dst) = val[i];
+    }
+  }
 }
 
 template <bool kFp8>
@@ -227,6 +234,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     mbar_init(&bars->mrg_a, 4);
     mbar_init(&bars->mrg_b, 1);
     mbar_init(&bars->mrg_c, 4);
+    mbar_init(&bars->mrg_d, 4);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -595,7 +603,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
     const int q4 = warp & 3;
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0;
+    uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0, mrg_d_ph = 0;
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       if (!it.ok) continue;
@@ -644,6 +652,11 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         WAIT(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
         fence_after_sync();
       }
+      // O[row = lane][32 columns] per step: staged in this warp's 4 KB (128-byte
+      // row pitch, 16-byte units XOR-swizzled by row) and written back as whole
+      // row segments, 128 (fp32) or 64 (bf16) contiguous bytes per row.
+      uint8_t* stg = smem + kOffEpi + (warp - kWarpRow0) * 4096;
+      const bool f32 = dst_f32 != nullptr;
       for (int c = 0; c < kDv / 32; ++c) {
         float v[32];
         if (nt > 0) {
@@ -656,7 +669,22 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
         }
-        if (live) store_row32(p, dst_f32, row, 32 * c, v);
+        if (f32) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                           pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+        }
+        __syncwarp();
+        if (f32) epi_rows_out<true>(stg, lane, q4, c, it, p);
+        else epi_rows_out<false>(stg, lane, q4, c, it, p);
+        __syncwarp();
       }
       if (live) {
         if (it.slot >= 0) p.part_lse[(int64_t)it.slot * kRows + r] = lse;
@@ -691,47 +719,47 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
           const int B = p.batch;
           const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
           const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
-          // pass 1: per-row max and normaliser (thread = row)
-          if (live) {
+          // pass 1 (thread = row): max, normaliser and the weight of every split,
+          // kept in the epilogue staging area as w[s][row]
+          float* wts = reinterpret_cast<float*>(smem + kOffEpi);
+          {
             float M = -INFINITY;
-            for (int s = 0; s < it.S; ++s)
-              M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
+            if (live)
+              for (int s = 0; s < it.S; ++s)
+                M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
             float tot = 0.f;
             if (M != -INFINITY)
               for (int s = 0; s < it.S; ++s) {
                 const float ls = __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r);
-                tot += ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
+                const float e = ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
+                wts[s * kRows + r] = e;
+                tot += e;
               }
-            bars->merge_m[r] = M;
-            bars->merge_inv[r] = M == -INFINITY ? 0.f : 1.f / tot;
-            p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
+            const float inv = M == -INFINITY ? 0.f : 1.f / tot;
+            for (int s = 0; s < it.S; ++s) wts[s * kRows + r] = M == -INFINITY ? 0.f : wts[s * kRows + r] * inv;
+            if (live) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->mrg_c);
           WAIT(&bars->mrg_c, mrg_c_ph, 45);
           mrg_c_ph ^= 1;
-          // pass 2: thread t owns float4 column t of every row; 8 rows in flight
+          // pass 2: thread t owns float4 column t of every row; 16 rows in flight
           const int c4 = tid - kWarpRow0 * 32;
-          for (int rb = 0; rb < it.nrows; rb += 8) {
-            float4 acc[8];
+          for (int rb = 0; rb < it.nrows; rb += 16) {
+            float4 acc[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < 16; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int s = 0; s < it.S; ++s) {
               const int slot = pbase + s * G + it.g;
-              float ls[8];
-              float4 ov[8];
+              float4 ov[16];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
+              for (int k = 0; k < 16; ++k) {
                 const int rr = min(rb + k, it.nrows - 1);
-                ls[k] = __ldcg(p.part_lse + (int64_t)slot * kRows + rr);
                 ov[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + rr) * kDv) + c4);
               }
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int rr = min(rb + k, it.nrows - 1);
-                const float M = bars->merge_m[rr];
-                const float w = (ls[k] == -INFINITY || M == -INFINITY) ? 0.f
-                                : ex2((ls[k] - M) * 1.4426950408889634f) * bars->merge_inv[rr];
+              for (int k = 0; k < 16; ++k) {
+                const float w = wts[s * kRows + min(rb + k, it.nrows - 1)];
                 acc[k].x += w * ov[k].x;
                 acc[k].y += w * ov[k].y;
                 acc[k].z += w * ov[k].z;
@@ -739,7 +767,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
               }
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
               if (rb + k >= it.nrows) break;
               const int64_t orow = it.q_row_base + it.row0 + rb + k;
               if (p.out_fp32) {
@@ -753,6 +781,11 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
             }
           }
           if (tid == kWarpRow0 * 32) p.counters[it.group] = 0;
+          // the weights live where the next epilogue stages its rows
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->mrg_d);
+          WAIT(&bars->mrg_d, mrg_d_ph, 46);
+          mrg_d_ph ^= 1;
         }
       }
     }
