@@ -79,12 +79,12 @@ def algorithmic_bytes(w) -> int:
     return nnz * 576 * elem + 4 * nnz + rows * (576 * 2 + 512 * 2 + 4)
 
 
-def ncu_traffic(config: str):
-    """DRAM bytes of one decode launch from the committed ncu capture, only if the
-    kernel source is the one that was profiled; else None."""
+def ncu_traffic(config: str, record: str = "ncu_traffic.json"):
+    """DRAM bytes of one launch from a committed ncu capture, only if the kernel
+    source is the one that was profiled; else None."""
     import hashlib
     try:
-        d = json.load(open(os.path.join(ROOT, "profiles", "ncu_traffic.json")))
+        d = json.load(open(os.path.join(ROOT, "profiles", record)))
         src = open(os.path.join(ROOT, d["kernel_source"]), "rb").read()
         if hashlib.sha256(src).hexdigest()[:16] != d["kernel_source_sha256_16"]:
             return None
@@ -237,6 +237,135 @@ def whole_job_rate(units_per_rank: int, world: int, ms_slowest: float) -> float:
     return world * units_per_rank / (ms_slowest * 1e-3)
 
 
+# ----------------------------------------------------------------------------- KV-cache write
+
+CW_METRIC = "MLA KV-cache write: tokens/s and achieved HBM GB/s on 1 GB300"
+CW_TOKENS, CW_SLOTS = 65536, 131072      # the draft block's whole KV, into its 131072-slot pool
+
+
+def cache_write_bytes(n: int, pool_fp8: bool) -> int:
+    """Algorithmic bytes: bf16 inputs (576 x 2 B) read, the pool row written, the slot read."""
+    return n * (576 * 2 + 576 * (1 if pool_fp8 else 2) + 4)
+
+
+def cache_write_main(args, rank: int, world: int):
+    """One step = one mla_cache_write of CW_TOKENS bf16 tokens into the pool."""
+    fp8 = args.config == "cache_write_fp8"
+    kv_dtype = "fp8" if fp8 else "bf16"
+    inp = mi.cache_write_inputs(CW_TOKENS, CW_SLOTS)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import cache_write as cw
+        n = 4096
+        pool = np.zeros((CW_SLOTS, 576), np.uint8 if fp8 else np.uint16)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            cw.cache_write(pool, inp.kv_c[:n], inp.k_pe[:n], inp.slot_mapping[:n], kv_dtype, inp.kv_scale)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        value = n * len(times) / sum(times)
+        print(json.dumps({"impl": "reference", "metric": CW_METRIC, "value": value, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f32->" + kv_dtype, "data": "synthetic",
+                          "config": {"workload": args.config, "sample": f"{n} of {CW_TOKENS} tokens per step"},
+                          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"{n} tokens per step"},
+                          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    import token_mla_paged_gb300 as m
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_index = torch.cuda.current_device()
+    kv_c = torch.from_numpy(inp.kv_c_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    k_pe = torch.from_numpy(inp.k_pe_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    slots = torch.from_numpy(inp.slot_mapping).cuda()
+    pool = torch.zeros(CW_SLOTS, 576, dtype=torch.uint8 if fp8 else torch.int16, device="cuda")
+    code = m.MLA_KV_FP8_E4M3 if fp8 else m.MLA_KV_BF16
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.mla_cache_write(kv_c, k_pe, slots, pool, code, inp.kv_scale)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world, device="cuda")
+    # end to end: the step's activations and slots from pinned host memory, the
+    # write, and one written row read back as the completion check
+    kc_h, kp_h, sl_h = kv_c.cpu().pin_memory(), k_pe.cpu().pin_memory(), slots.cpu().pin_memory()
+    row_h = torch.empty(576, dtype=pool.dtype).pin_memory()
+    first = int(inp.slot_mapping[0])
+    h2d = (kc_h.numel() + kp_h.numel()) * 2 + sl_h.numel() * 4
+    d2h = row_h.numel() * row_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        kv_c.copy_(kc_h, non_blocking=True)
+        k_pe.copy_(kp_h, non_blocking=True)
+        slots.copy_(sl_h, non_blocking=True)
+        step()
+        row_h.copy_(pool[first], non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps, world, device="cuda")
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks = load_peaks()
+    nbytes = cache_write_bytes(CW_TOKENS, fp8)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        from oracle import cache_write as cw
+        n = 4096
+        t0 = time.perf_counter()
+        cw.cache_write(np.zeros((CW_SLOTS, 576), np.uint8 if fp8 else np.uint16), inp.kv_c[:n], inp.k_pe[:n],
+                       inp.slot_mapping[:n], kv_dtype, inp.kv_scale)
+        cpu = {"value": n / (time.perf_counter() - t0), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {CW_TOKENS} tokens"}
+    traffic = ncu_traffic(args.config, "ncu_traffic_cache_write.json")
+    print(json.dumps({
+        "metric": CW_METRIC, "value": whole_job_rate(CW_TOKENS, world, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->" + kv_dtype, "data": "synthetic",
+        "config": {"workload": args.config, "tokens": CW_TOKENS, "pool_slots": CW_SLOTS, "kv_dtype": kv_dtype,
+                   "l2": "flushed (256 MB write) between timed steps"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peaks["source"],
+                     "alg_bytes": nbytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": whole_job_rate(CW_TOKENS, world, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps, "clocks": clk.summary()}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -245,7 +374,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="draft_block_bf16", choices=mi.CONFIG_NAMES)
+    ap.add_argument("--config", default="draft_block_bf16", choices=mi.CONFIG_NAMES + mi.EXTRA_CONFIG_NAMES)
     ap.add_argument("--algo", default="tensor", choices=["tensor", "cuda_core"])
     ap.add_argument("--workers", type=int, default=0, help="plan workers (0 = kernel default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -254,6 +383,8 @@ def main():
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.config in mi.EXTRA_CONFIG_NAMES:
+        return cache_write_main(args, rank, world)
 
     if args.impl == "reference":
         if rank != 0:

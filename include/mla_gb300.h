@@ -213,6 +213,44 @@ mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const fl
  * *info its detail; returns MLA_ERR_DEVICE_FAULT when *code != 0. */
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info);
 
+/* Dtype of an activation input to mla_cache_write. */
+typedef enum { MLA_ACT_BF16 = 0, MLA_ACT_FP32 = 1 } mla_act_dtype;
+
+/* Arguments of one KV-cache write.  All pointers are device pointers. */
+typedef struct {
+  const void* kv_c;             /* [num_tokens, 512] latent columns, rows kv_c_stride elements apart */
+  int32_t kv_c_dtype;           /* mla_act_dtype */
+  int64_t kv_c_stride;          /* >= 512 */
+  const void* k_pe;             /* [num_tokens, 64] RoPE columns, rows k_pe_stride elements apart */
+  int32_t k_pe_dtype;           /* mla_act_dtype */
+  int64_t k_pe_stride;          /* >= 64 */
+  const int32_t* slot_mapping;  /* [num_tokens] pool slot of each token; < 0 = padding */
+  int64_t num_tokens;           /* >= 0 */
+  void* kv_pool;                /* bf16 | fp8 [num_slots, 576], the pool mla_decode_fwd reads */
+  int64_t num_slots;            /* > 0 */
+  int32_t kv_dtype;             /* mla_kv_dtype of the pool */
+  float kv_scale;               /* fp8: finite, > 0 (stored = value / kv_scale); ignored for bf16 */
+} mla_cache_write_args;
+
+/* KV-cache write, the step before the decode: each new token's 512 latent and 64
+ * RoPE columns become one 576-wide row of the pool at its slot ("[ROCm] Dspark
+ * MLA module", Details: the decode KV-cache write, concat_and_cache_mla, bf16 or
+ * fp8 with a per-tensor scale).  For token n with 0 <= slot_mapping[n] < num_slots:
+ *   row = (kv_c[n, 0:512], k_pe[n, 0:64]) as float32 (bf16 widens exactly);
+ *   bf16 pool: pool[slot] = row rounded to bf16 (nearest, ties to even);
+ *   fp8 pool:  pool[slot] = e4m3fn(row * fp32(1/kv_scale)), each product rounded
+ *              to float32, then to nearest e4m3fn (ties to even), magnitudes
+ *              above 448 saturated to +-448.
+ * Tokens with a negative slot (padding) or a slot >= num_slots are skipped.  A
+ * slot named twice in one call holds one of the rows (unspecified which).  Each
+ * input carries its own dtype and is converted, never reinterpreted: the pages
+ * report an fp32 k_pe silently read as bf16 at this step (same page, review
+ * comment), so a dtype outside mla_act_dtype is MLA_ERR_INVALID_ARG.  Inputs
+ * need 16-byte aligned rows (base pointers 16-byte aligned, strides a multiple
+ * of 8 bf16 / 4 fp32 elements), else MLA_ERR_INVALID_ARG.  Enqueued on `stream`;
+ * nothing is read back, so the call can be captured in a CUDA graph. */
+mla_status mla_cache_write(const mla_cache_write_args* args, void* stream);
+
 /* Forward call for callers that cannot allocate device memory (a runtime or
  * allocator that hands out only input and output tensors): the plan buffer and
  * the workspace come from one static device array of 16 MiB inside the library

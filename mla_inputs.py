@@ -280,6 +280,49 @@ def flatten_block(w: Workload) -> Workload:
 
 
 CONFIG_NAMES = ["tiny_causal_bf16", "draft_block_bf16", "verify_fp8", "long_skewed_fp8", "cp_shards_bf16"]
+# the KV-cache write that precedes the decode (a separate call, measured on its own)
+EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16"]
+
+
+@dataclasses.dataclass
+class CacheWriteInputs:
+    """New tokens' activations and their slots.  kv_c / k_pe are float32 arrays of
+    the input values; with bf16 inputs they hold bf16-representable values and
+    kv_c_bits / k_pe_bits hold the bf16 patterns."""
+    kv_c: np.ndarray
+    k_pe: np.ndarray
+    kv_c_bits: Optional[np.ndarray]
+    k_pe_bits: Optional[np.ndarray]
+    slot_mapping: np.ndarray
+    num_slots: int
+    kv_scale: float
+
+
+def cache_write_inputs(num_tokens: int, num_slots: int, *, kv_c_dtype: str = "bf16", k_pe_dtype: str = "bf16",
+                       seed: int = SEED_BASE + 6, padding: float = 0.0, out_of_range: float = 0.0,
+                       spread: bool = False) -> CacheWriteInputs:
+    """Seeded inputs: values N(0,1) (with spread=True a mix of magnitudes from 1e-5 to
+    40, so fp8 at kv_scale 0.05 sees subnormals and saturation), slots a seeded
+    permutation prefix of the pool, a fraction replaced by -1 (padding) or by
+    slots past the end."""
+    rng = np.random.default_rng(seed)
+    assert num_tokens <= num_slots
+    def draw(shape, dtype):
+        x = rng.standard_normal(shape).astype(np.float32)
+        if spread:
+            x *= rng.choice(np.array([1e-5, 1e-3, 0.05, 1.0, 10.0, 40.0], np.float32), size=shape)
+        if dtype == "bf16":
+            bits = to_bf16_bits(x)
+            return (bits.astype(np.uint32) << 16).view(np.float32), bits
+        return x, None
+    kv_c, kv_c_bits = draw((num_tokens, 512), kv_c_dtype)
+    k_pe, k_pe_bits = draw((num_tokens, 64), k_pe_dtype)
+    slots = rng.permutation(num_slots)[:num_tokens].astype(np.int32)
+    u = rng.random(num_tokens)
+    slots[u < padding] = -1
+    slots[(u >= padding) & (u < padding + out_of_range)] = num_slots + rng.integers(0, 1000)
+    return CacheWriteInputs(kv_c=kv_c, k_pe=k_pe, kv_c_bits=kv_c_bits, k_pe_bits=k_pe_bits,
+                            slot_mapping=slots, num_slots=num_slots, kv_scale=FP8_KV_SCALE)
 
 
 # ----------------------------------------------------------------------------

@@ -154,3 +154,37 @@ def test_fwd_rejects_bad_arguments_before_touching_the_device():
     a.q = 18
     assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1      # misaligned q
     assert lib.mla_merge_states(None, 0, None, 0, 1, 512, None, 0, None, None) == 1
+
+
+def test_cache_write_rejects_bad_arguments_before_touching_the_device():
+    """mla_cache_write validates dtypes, sizes, strides and alignment on the host;
+    an empty call returns before any CUDA work."""
+    import ctypes
+    lib = m.library()
+
+    def args(**kw):
+        a = m.CacheWriteArgs()
+        a.kv_c, a.kv_c_dtype, a.kv_c_stride = 0x10000, m.MLA_ACT_BF16, 512
+        a.k_pe, a.k_pe_dtype, a.k_pe_stride = 0x20000, m.MLA_ACT_BF16, 64
+        a.slot_mapping, a.num_tokens = 0x30000, 0
+        a.kv_pool, a.num_slots, a.kv_dtype, a.kv_scale = 0x40000, 16, m.MLA_KV_FP8_E4M3, 0.05
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return ctypes.byref(a)
+
+    assert lib.mla_cache_write(args(), None) == 0                      # nothing to write
+    assert lib.mla_cache_write(None, None) == 1
+    assert lib.mla_cache_write(args(kv_c_dtype=2), None) == 1          # not an activation dtype
+    assert lib.mla_cache_write(args(k_pe_dtype=-1), None) == 1
+    assert lib.mla_cache_write(args(kv_dtype=2), None) == 1
+    assert lib.mla_cache_write(args(kv_scale=0.0), None) == 1          # fp8 needs a scale
+    assert lib.mla_cache_write(args(kv_scale=float("nan")), None) == 1
+    assert lib.mla_cache_write(args(num_tokens=-1), None) == 1
+    assert lib.mla_cache_write(args(num_slots=0), None) == 1
+    assert lib.mla_cache_write(args(kv_c_stride=511), None) == 1
+    assert lib.mla_cache_write(args(k_pe_stride=63), None) == 1
+    # with tokens to write: null, misaligned or non-16-byte strides are refused
+    assert lib.mla_cache_write(args(num_tokens=4, kv_c=None), None) == 1
+    assert lib.mla_cache_write(args(num_tokens=4, k_pe=0x20008), None) == 1
+    assert lib.mla_cache_write(args(num_tokens=4, kv_c_stride=516), None) == 1
+    assert lib.mla_cache_write(args(num_tokens=4, k_pe_dtype=m.MLA_ACT_FP32, k_pe_stride=66), None) == 1

@@ -23,6 +23,7 @@ MLA_KV_BF16, MLA_KV_FP8_E4M3 = 0, 1
 MLA_OUT_BF16, MLA_OUT_FP32 = 0, 1
 MLA_PLAN_STATIC, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST = 0, 1, 2
 MLA_ALGO_TENSOR, MLA_ALGO_CUDA_CORE = 0, 1
+MLA_ACT_BF16, MLA_ACT_FP32 = 0, 1
 D_QK, D_V = 576, 512
 
 DEVICE_ERRORS = {0: "ok", 1: "kv index out of range", 2: "decreasing indptr",
@@ -57,6 +58,14 @@ class FwdArgs(ctypes.Structure):
                 ("ws_bytes", ctypes.c_size_t)]
 
 
+class CacheWriteArgs(ctypes.Structure):
+    _fields_ = [("kv_c", ctypes.c_void_p), ("kv_c_dtype", ctypes.c_int32), ("kv_c_stride", ctypes.c_int64),
+                ("k_pe", ctypes.c_void_p), ("k_pe_dtype", ctypes.c_int32), ("k_pe_stride", ctypes.c_int64),
+                ("slot_mapping", ctypes.c_void_p), ("num_tokens", ctypes.c_int64),
+                ("kv_pool", ctypes.c_void_p), ("num_slots", ctypes.c_int64), ("kv_dtype", ctypes.c_int32),
+                ("kv_scale", ctypes.c_float)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; "
@@ -73,6 +82,7 @@ def _load():
         "mla_decode_fwd": (ctypes.c_int, [ctypes.POINTER(FwdArgs), vp]),
         "mla_decode_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FwdArgs), vp]),
         "mla_merge_states": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, i32, vp, vp]),
+        "mla_cache_write": (ctypes.c_int, [ctypes.POINTER(CacheWriteArgs), vp]),
         "mla_get_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
@@ -87,7 +97,7 @@ _lib = _load()
 # Symbols the header declares; tests check the library exports each one.
 ABI_SYMBOLS = ("mla_abi_version", "mla_status_string", "mla_decode_plan_size", "mla_decode_plan",
                "mla_decode_plan_device", "mla_decode_fwd", "mla_merge_states",
-               "mla_get_device_error", "mla_decode_fwd_noalloc")
+               "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write")
 
 
 def library():
@@ -197,6 +207,39 @@ def mla_merge_states(o_parts, lse_parts, o, lse, stream=None) -> None:
                                  MLA_OUT_FP32 if o.dtype == torch.float32 else MLA_OUT_BF16,
                                  _ptr(lse), _stream(stream)),
            "mla_merge_states")
+
+
+def _act_dtype(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return MLA_ACT_BF16
+    if t.dtype == torch.float32:
+        return MLA_ACT_FP32
+    raise MlaError(1, f"mla_cache_write: unsupported activation dtype {t.dtype}")
+
+
+def mla_cache_write(kv_c, k_pe, slot_mapping, kv_pool, kv_dtype: int, kv_scale: float = 1.0,
+                    stream=None) -> None:
+    """kv_c [n, 512] and k_pe [n, 64] (bf16 or fp32, unit stride along the row,
+    k_pe may also be [n, 1, 64]); slot_mapping int32 [n]; kv_pool [slots, 576]."""
+    if k_pe.dim() == 3:
+        k_pe = k_pe.reshape(k_pe.shape[0], k_pe.shape[-1])
+    if kv_c.stride(-1) != 1 or k_pe.stride(-1) != 1:
+        raise MlaError(1, "mla_cache_write: rows must be contiguous along the columns")
+    a = CacheWriteArgs()
+    a.kv_c = _ptr(kv_c)
+    a.kv_c_dtype = _act_dtype(kv_c)
+    a.kv_c_stride = kv_c.stride(0)
+    a.k_pe = _ptr(k_pe)
+    a.k_pe_dtype = _act_dtype(k_pe)
+    a.k_pe_stride = k_pe.stride(0)
+    a.slot_mapping = _ptr(slot_mapping)
+    a.num_tokens = int(slot_mapping.shape[0])
+    a.kv_pool = _ptr(kv_pool)
+    a.num_slots = int(kv_pool.shape[0])
+    a.kv_dtype = kv_dtype
+    a.kv_scale = kv_scale
+    _check(_lib.mla_cache_write(ctypes.byref(a), _stream(stream)), "mla_cache_write")
 
 
 def mla_get_device_error(workspace_d, stream=None) -> Tuple[int, int]:

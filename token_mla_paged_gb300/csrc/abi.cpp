@@ -169,6 +169,25 @@ mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const fl
                              o_dtype == MLA_OUT_FP32, lse, stream);
 }
 
+mla_status mla_cache_write(const mla_cache_write_args* a, void* stream) {
+  if (!a) return MLA_ERR_INVALID_ARG;
+  if (a->kv_c_dtype != MLA_ACT_BF16 && a->kv_c_dtype != MLA_ACT_FP32) return MLA_ERR_INVALID_ARG;
+  if (a->k_pe_dtype != MLA_ACT_BF16 && a->k_pe_dtype != MLA_ACT_FP32) return MLA_ERR_INVALID_ARG;
+  if (a->kv_dtype != MLA_KV_BF16 && a->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (a->num_tokens < 0 || a->num_slots <= 0) return MLA_ERR_INVALID_ARG;
+  if (a->kv_c_stride < 512 || a->k_pe_stride < 64) return MLA_ERR_INVALID_ARG;
+  if (a->kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(a->kv_scale) && a->kv_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (a->num_tokens == 0) return MLA_OK;
+  if (!a->kv_c || !a->k_pe || !a->slot_mapping || !a->kv_pool) return MLA_ERR_INVALID_ARG;
+  // 16-byte rows: aligned bases, strides a whole number of 16-byte units
+  const int64_t c_unit = a->kv_c_dtype == MLA_ACT_FP32 ? 4 : 8, pe_unit = a->k_pe_dtype == MLA_ACT_FP32 ? 4 : 8;
+  if (!aligned(a->kv_c, 16) || !aligned(a->k_pe, 16) || !aligned(a->kv_pool, 16) || !aligned(a->slot_mapping, 4) ||
+      a->kv_c_stride % c_unit != 0 || a->k_pe_stride % pe_unit != 0)
+    return MLA_ERR_INVALID_ARG;
+  return launch_cache_write(*a, stream);
+}
+
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info) {
   if (!workspace_d || !code) return MLA_ERR_INVALID_ARG;
   int32_t h[2] = {0, 0};

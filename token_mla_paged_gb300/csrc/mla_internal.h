@@ -114,6 +114,7 @@ mla_status launch_decode_tensor(const DecodeParams& dp, void* stream);
 mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const float* lse_parts,
                                int n, int64_t rows, int dv, void* o, int o_fp32, float* lse,
                                void* stream);
+mla_status launch_cache_write(const mla_cache_write_args& a, void* stream);
 int tensor_kernel_available();
 
 }  // namespace mla
