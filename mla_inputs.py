@@ -52,6 +52,8 @@ class Workload:
     pos_stride: int = 1
     pos_base_per_req: Optional[np.ndarray] = None   # int32 [B]
     g_kv_indptr: Optional[np.ndarray] = None        # int32 [B+1]
+    kv_pos: Optional[np.ndarray] = None             # int32 [nnz] global position of each entry
+    window: int = 0                                 # sliding window (causal only), 0 = none
     meta: dict = dataclasses.field(default_factory=dict)
 
     @property
@@ -280,6 +282,56 @@ def flatten_block(w: Workload) -> Workload:
 
 
 CONFIG_NAMES = ["tiny_causal_bf16", "draft_block_bf16", "verify_fp8", "long_skewed_fp8", "cp_shards_bf16"]
+def sparse_variant(kind: str, *, batch: int, num_heads: int, q_lens, global_lens, window: int = 128,
+                   topk: int = 2048, ratio: int = 128, kv_dtype: str = "fp8", seed: int = SEED_BASE + 7,
+                   num_slots: Optional[int] = None) -> Workload:
+    """Index lists of the DSV4 layer types over a page-size-1 pool, every entry with
+    its global position (kv_pos), causal on global positions (g_kv_indptr = the
+    requests' real lengths Lg).  Token t of a T-token block sits at Lg - T + t.
+      swa: the positions a T-token block can see through a sliding window W,
+           [Lg - T - W + 1, Lg); the decode applies the window (window = W).
+      csa: the window's positions plus `topk` distinct positions drawn (seeded,
+           uniformly) from the older ones, sorted; no window bound.
+      hca: one compressed entry per complete block of `ratio` positions before the
+           window (its position is the block's last), then the window's
+           positions; no window bound.
+    Pool rows are N(0,1) latent rows (compressed entries are just more rows)."""
+    rng = np.random.default_rng(seed)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    Lg = np.asarray(global_lens, dtype=np.int64)
+    pos_lists = []
+    for b in range(batch):
+        T, L = int(q_lens[b]), int(Lg[b])
+        w0 = max(0, L - T - window + 1)
+        win = np.arange(w0, L, dtype=np.int64)
+        if kind == "swa":
+            pos = win
+        elif kind == "csa":
+            k = min(topk, w0)
+            pos = np.sort(np.concatenate([rng.choice(w0, size=k, replace=False), win]))
+        elif kind == "hca":
+            nblk = w0 // ratio
+            pos = np.concatenate([np.arange(nblk, dtype=np.int64) * ratio + ratio - 1, win])
+        else:
+            raise ValueError(kind)
+        pos_lists.append(pos)
+    lens = np.array([len(p) for p in pos_lists], dtype=np.int64)
+    nnz = int(lens.sum())
+    if num_slots is None:
+        num_slots = max(1, _pow2_at_least(nnz))
+    kv_scale = FP8_KV_SCALE if kv_dtype == "fp8" else 1.0
+    kv_indices = rng.permutation(num_slots)[:nnz].astype(np.int32)
+    total_q = int(q_lens.sum())
+    q_bits = to_bf16_bits(rng.standard_normal((total_q, num_heads, D_QK), dtype=np.float32))
+    kv_bits = _normal_bits(rng, (num_slots, D_QK), kv_dtype, kv_scale)
+    return Workload(name=f"{kind}_{kv_dtype}", num_heads=num_heads, q_bits=q_bits, kv_bits=kv_bits,
+                    kv_dtype=kv_dtype, kv_indptr=_indptr(lens), kv_indices=kv_indices,
+                    qo_indptr=_indptr(q_lens), causal=True, softmax_scale=SOFTMAX_SCALE,
+                    kv_scale=float(kv_scale), g_kv_indptr=_indptr(Lg),
+                    kv_pos=np.concatenate(pos_lists).astype(np.int32) if nnz else np.zeros(0, np.int32),
+                    window=window if kind == "swa" else 0)
+
+
 # the KV-cache write that precedes the decode (a separate call, measured on its own)
 EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16"]
 
@@ -346,4 +398,5 @@ def to_device(w: Workload, device="cuda") -> dict:
                 kv_indptr=i32(w.kv_indptr), kv_indices=i32(w.kv_indices), qo_indptr=i32(w.qo_indptr),
                 causal=w.causal, softmax_scale=w.softmax_scale, kv_scale=w.kv_scale,
                 pos_base=w.pos_base, pos_stride=w.pos_stride,
-                pos_base_per_req=i32(w.pos_base_per_req), g_kv_indptr=i32(w.g_kv_indptr))
+                pos_base_per_req=i32(w.pos_base_per_req), g_kv_indptr=i32(w.g_kv_indptr),
+                kv_pos=i32(w.kv_pos), window=int(w.window))

@@ -11,6 +11,8 @@ For request b with local KV length L_b, query tokens T_b and head h:
             (kappa = kv_scale for an fp8 pool, 1 for bf16)
   s_i     = sigma * <q[t, h, 0:576], k_i[0:576]>                    sigma = softmax_scale
   V_t     = { i : not causal  or  g_b(i) <= Lg_b - T_b + t },  g_b(i) = base_b + i * stride
+            (g_b(i) = kv_pos[kv_indptr[b] + i] when per-entry positions are given;
+             with a window W > 0, causal rows also need g_b(i) > Lg_b - T_b + t - W)
   LSE     = ln sum_{i in V_t} exp(s_i)                              (natural log)
   O       = sum_{i in V_t} exp(s_i - LSE) * k_i[0:512]
   empty V_t:  O = 0, LSE = -inf
@@ -29,9 +31,17 @@ Sources on the pages:
     with the global lengths carried by g_kv_indptr and an LSE output --
     "Speculative decode + DCP on gfx1250", Problem;
   * per-tensor fp8 scale -- "[ROCm][Spec Decode] ...", section "Three pieces".
+  * index lists other than the whole committed KV: one plan per layer type --
+    a sliding window (SWA), a window plus top-k selected entries (CSA), a
+    window plus one compressed entry per 128 tokens (HCA) -- over the same
+    decode ("[DSV4] Tuned ASM FP8 decode with split plans; HCA on aiter's
+    persistent V4-NM kernel", Summary part 1).  Such lists are not a run of
+    positions base + i*stride, so each entry can carry its global position
+    (kv_pos), and the sliding window is a lower bound on visible positions.
 The exact causal limit (token t of a T-token block sees global positions up to
-Lg - T + t), the 576/512 widths and the natural-log LSE are this build's
-readings where the pages are silent.
+Lg - T + t), the window reading (positions in (limit - W, limit]), the 576/512
+widths and the natural-log LSE are this build's readings where the pages are
+silent.
 
 Computation uses max subtraction and processes query rows in chunks so memory
 stays bounded; the chunking is exact (each row is independent).
@@ -50,17 +60,22 @@ D_V = 512
 
 
 def visible_mask(L: int, T: int, t_of_row: np.ndarray, causal: bool, base: int, stride: int,
-                 Lg: int) -> np.ndarray:
+                 Lg: int, pos: Optional[np.ndarray] = None, window: int = 0) -> np.ndarray:
     """Boolean [rows, L]: entry i is visible to the row's token t.
 
-    Non-causal: all L entries.  Causal: global position base + i*stride must not
-    exceed Lg - T + t.
+    Non-causal: all L entries.  Causal: the entry's global position (pos[i] when
+    given, else base + i*stride) must not exceed limit = Lg - T + t, and with a
+    window W > 0 must also exceed limit - W.
     """
     if not causal:
         return np.ones((t_of_row.shape[0], L), dtype=bool)
-    g = base + stride * np.arange(L, dtype=np.int64)
+    g = (np.asarray(pos, dtype=np.int64) if pos is not None
+         else base + stride * np.arange(L, dtype=np.int64))
     limit = (Lg - T + t_of_row.astype(np.int64))[:, None]
-    return g[None, :] <= limit
+    vis = g[None, :] <= limit
+    if window > 0:
+        vis &= g[None, :] > limit - window
+    return vis
 
 
 def attend_rows(qrows: np.ndarray, K: np.ndarray, vis: np.ndarray,
@@ -93,7 +108,8 @@ def mla_decode(q_bits: np.ndarray, kv_bits: np.ndarray, kv_dtype: str,
                pos_base: int = 0, pos_stride: int = 1,
                pos_base_per_req: Optional[np.ndarray] = None,
                g_kv_indptr: Optional[np.ndarray] = None,
-               requests=None, row_chunk: int = 64) -> Tuple[np.ndarray, np.ndarray]:
+               requests=None, row_chunk: int = 64, kv_pos: Optional[np.ndarray] = None,
+               window: int = 0) -> Tuple[np.ndarray, np.ndarray]:
     """Reference MLA decode.  Returns O float64 [total_q, H, 512] and LSE float64 [total_q, H].
 
     ``requests`` restricts the work to a subset of request indices (rows of the
@@ -122,7 +138,8 @@ def mla_decode(q_bits: np.ndarray, kv_bits: np.ndarray, kv_dtype: str,
         lse_b = np.empty(T * H)
         for r0 in range(0, T * H, row_chunk):
             r1 = min(T * H, r0 + row_chunk)
-            vis = visible_mask(L, T, t_of_row[r0:r1], causal, base, pos_stride, Lg)
+            vis = visible_mask(L, T, t_of_row[r0:r1], causal, base, pos_stride, Lg,
+                               None if kv_pos is None else kv_pos[k0:k1], window)
             o_b[r0:r1], lse_b[r0:r1] = attend_rows(qrows[r0:r1], K, vis, softmax_scale)
         O[q0:q1] = o_b.reshape(T, H, D_V)
         LSE[q0:q1] = lse_b.reshape(T, H)
@@ -133,7 +150,7 @@ def mla_decode_workload(w, **kw) -> Tuple[np.ndarray, np.ndarray]:
     """Convenience wrapper over a ``mla_inputs.Workload``."""
     return mla_decode(w.q_bits, w.kv_bits, w.kv_dtype, w.kv_indptr, w.kv_indices, w.qo_indptr,
                       w.causal, w.softmax_scale, w.kv_scale, w.pos_base, w.pos_stride,
-                      w.pos_base_per_req, w.g_kv_indptr, **kw)
+                      w.pos_base_per_req, w.g_kv_indptr, kv_pos=w.kv_pos, window=w.window, **kw)
 
 
 def merge_states(o_parts: np.ndarray, lse_parts: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:

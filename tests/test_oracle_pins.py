@@ -378,8 +378,8 @@ def test_pins_catch_an_off_by_one_causal_limit(monkeypatch):
     """Plant an off-by-one in the oracle's mask; the closed-form pin must fail."""
     orig = mo.visible_mask
 
-    def wrong(L, T, t_of_row, causal, base, stride, Lg):
-        return orig(L, T, t_of_row, causal, base, stride, Lg - 1)
+    def wrong(L, T, t_of_row, causal, base, stride, Lg, pos=None, window=0):
+        return orig(L, T, t_of_row, causal, base, stride, Lg - 1, pos, window)
 
     monkeypatch.setattr(mo, "visible_mask", wrong)
     with pytest.raises(AssertionError):
