@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 2
+#define MLA_ABI_VERSION 3
 #define MLA_D_QK 576             /* latent 512 + RoPE 64 */
 #define MLA_D_V 512
 #define MLA_ROWS_PER_GROUP 128   /* query rows (t,h) handled together */
@@ -164,6 +164,16 @@ typedef struct {
   size_t plan_bytes;
   void* workspace_d;                 /* device workspace, >= the size mla_decode_plan_size gives */
   size_t ws_bytes;
+  /* Index lists that are not a run of positions (since ABI version 3): one index
+   * list per layer type -- a sliding window (SWA), a window plus top-k selected
+   * entries (CSA), a window plus one compressed entry per 128 tokens (HCA) --
+   * over the same decode ("[DSV4] Tuned ASM FP8 decode with split plans; HCA on
+   * aiter's persistent V4-NM kernel", Summary part 1). */
+  const int32_t* kv_pos;             /* nullable [nnz]: global position of each entry, ascending
+                                        within a request; replaces pos_base + i*pos_stride */
+  int32_t window;                    /* >= 0; causal only: with W > 0 token t also needs
+                                        position > Lg - T + t - W (sliding window); 0 = none */
+  int32_t reserved2;                 /* 0 */
 } mla_fwd_args;
 
 /* ABI version (MLA_ABI_VERSION); lets a caller probe capabilities by number

@@ -140,6 +140,12 @@ def test_fwd_rejects_bad_arguments_before_touching_the_device():
     a.pos_stride = 0
     assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1
     a.pos_stride = 1
+    a.window = -1
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1      # negative window
+    a.window = 0
+    a.kv_pos = 18
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1      # misaligned positions
+    a.kv_pos = None
     a.num_slots = 10
     a.q = a.kv_pool = a.kv_indptr = a.kv_indices = a.qo_indptr = a.o = a.lse = 16
     a.plan_d = 256

@@ -55,7 +55,8 @@ class FwdArgs(ctypes.Structure):
                 ("kv_scale", ctypes.c_float), ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
                 ("params", ctypes.POINTER(PlanParams)), ("plan_d", ctypes.c_void_p),
                 ("plan_bytes", ctypes.c_size_t), ("workspace_d", ctypes.c_void_p),
-                ("ws_bytes", ctypes.c_size_t)]
+                ("ws_bytes", ctypes.c_size_t), ("kv_pos", ctypes.c_void_p), ("window", ctypes.c_int32),
+                ("reserved2", ctypes.c_int32)]
 
 
 class CacheWriteArgs(ctypes.Structure):
@@ -168,7 +169,8 @@ def mla_decode_plan_device(params: PlanParams, kv_indptr, qo_indptr, plan_d, wor
 def mla_decode_fwd(*, q, kv_pool, kv_dtype: int, kv_indptr, kv_indices, qo_indptr, causal: bool,
                    softmax_scale: float, kv_scale: float, o, lse, params: PlanParams, plan_d,
                    workspace_d, pos_base: int = 0, pos_stride: int = 1, pos_base_per_req=None,
-                   g_kv_indptr=None, algo: int = MLA_ALGO_TENSOR, stream=None) -> None:
+                   g_kv_indptr=None, algo: int = MLA_ALGO_TENSOR, kv_pos=None, window: int = 0,
+                   stream=None) -> None:
     import torch
     out_dtype = MLA_OUT_FP32 if o.dtype == torch.float32 else MLA_OUT_BF16
     a = FwdArgs()
@@ -195,6 +197,8 @@ def mla_decode_fwd(*, q, kv_pool, kv_dtype: int, kv_indptr, kv_indices, qo_indpt
     a.plan_bytes = plan_d.numel() * plan_d.element_size()
     a.workspace_d = _ptr(workspace_d)
     a.ws_bytes = workspace_d.numel() * workspace_d.element_size()
+    a.kv_pos = _ptr(kv_pos)
+    a.window = int(window)
     _check(_lib.mla_decode_fwd(ctypes.byref(a), _stream(stream)), "mla_decode_fwd")
 
 

@@ -86,6 +86,7 @@ mla_status mla_decode_fwd(const mla_fwd_args* a, void* stream) {
   if (a->kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(a->kv_scale) && a->kv_scale > 0.f))
     return MLA_ERR_INVALID_ARG;
   if (a->pos_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (a->window < 0 || (a->kv_pos && !aligned(a->kv_pos, 4))) return MLA_ERR_INVALID_ARG;
   if (a->num_slots <= 0 || a->num_slots > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (p.batch > 0) {
     if (!a->q || !a->kv_pool || !a->kv_indptr || !a->kv_indices || !a->qo_indptr || !a->o ||
@@ -135,6 +136,8 @@ mla_status mla_decode_fwd(const mla_fwd_args* a, void* stream) {
   dp.causal = a->causal;
   dp.pos_base = a->pos_base;
   dp.pos_stride = a->pos_stride;
+  dp.kv_pos = a->kv_pos;
+  dp.window = a->window;
   dp.batch = p.batch;
   dp.num_heads = p.num_heads;
   dp.max_q_len = p.max_q_len;

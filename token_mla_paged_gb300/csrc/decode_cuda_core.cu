@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_cuda_core_kernel(Decod
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int c = cl + 8 * j;
-          vis[j] = row_live && s_valid[c] && visible(it, p.causal, (int64_t)(e + c), t_row);
+          vis[j] = row_live && s_valid[c] && visible(it, p, (int64_t)(e + c), t_row);
           sc[j] *= p.scale_log2;
           if (vis[j]) tmax = fmaxf(tmax, sc[j]);
         }

@@ -500,15 +500,24 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       if (lane == 0) mbar_arrive(&bars->q_full);
       ++qitem;
 
-      // Visibility: local entry i is visible to this row iff i < iend and its index is valid.
-      int iend = it.e1;
-      if (p.causal && live) {
-        const int t = (it.row0 + r) / p.num_heads;
-        const int64_t lim = it.Lg - it.T + t - it.base;
+      // Visibility: local entry i is visible to this row iff ibeg <= i < iend, its
+      // index is valid and, with per-entry positions, its position passes the
+      // row's causal limit (and window).
+      const int t_row = (it.row0 + r) / p.num_heads;
+      int ibeg = 0, iend = it.e1;
+      if (p.causal && live && !p.kv_pos) {
+        const int64_t lim = it.Lg - it.T + t_row - it.base;
         const int64_t cnt = lim < 0 ? 0 : lim / it.stride + 1;
         if (cnt < iend) iend = (int)cnt;
+        if (p.window > 0) {              // positions base + i*stride > limit - W
+          const int64_t lo = lim - p.window;
+          const int64_t first = lo < 0 ? 0 : lo / it.stride + 1;
+          ibeg = first < (int64_t)iend ? (int)first : iend;
+        }
       }
       if (!live) iend = -1;
+      // tokens of this warp's 32 rows (per-entry positions need one mask per token)
+      const int t_first = (it.row0 + 32 * q4) / p.num_heads, t_last = (it.row0 + 32 * q4 + 31) / p.num_heads;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++sseq, ++pseq) {
         const int sb = sseq & 1, pb = pseq % kPBufs;
@@ -526,8 +535,25 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
             const int32_t s = __ldg(p.kv_indices + it.kv_off + b);
             ok1 = s >= 0 && s < p.num_slots;
           }
-          vlo = __ballot_sync(0xffffffffu, ok0);
-          vhi = __ballot_sync(0xffffffffu, ok1);
+          if (p.kv_pos && p.causal) {
+            const int64_t g0 = a < it.e1 ? (int64_t)__ldg(p.kv_pos + it.kv_off + a) : INT64_MAX;
+            const int64_t g1 = b < it.e1 ? (int64_t)__ldg(p.kv_pos + it.kv_off + b) : INT64_MAX;
+            vlo = vhi = 0;
+            for (int t = t_first; t <= t_last; ++t) {
+              const int64_t lim = it.Lg - it.T + t;
+              const bool in0 = g0 <= lim && (p.window <= 0 || g0 > lim - p.window);
+              const bool in1 = g1 <= lim && (p.window <= 0 || g1 > lim - p.window);
+              const uint32_t m0 = __ballot_sync(0xffffffffu, ok0 && in0);
+              const uint32_t m1 = __ballot_sync(0xffffffffu, ok1 && in1);
+              if (t == t_row) {
+                vlo = m0;
+                vhi = m1;
+              }
+            }
+          } else {
+            vlo = __ballot_sync(0xffffffffu, ok0);
+            vhi = __ballot_sync(0xffffffffu, ok1);
+          }
         }
         WAIT(&bars->s_full[sb], (sseq >> 1) & 1, 31);
         fence_after_sync();
@@ -539,13 +565,20 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-        const int nvis = iend - i0;   // entries [0, nvis) of the tile may be visible
+        // entries [nbeg, nvis) of the tile may be visible: fold the range into the masks
+        {
+          const int nvis = iend - i0, nbeg = ibeg - i0;
+          const int hi = nvis < 0 ? 0 : (nvis > 64 ? 64 : nvis), lo = nbeg < 0 ? 0 : (nbeg > 64 ? 64 : nbeg);
+          const uint64_t range = (hi >= 64 ? ~0ull : ((1ull << hi) - 1)) & (lo >= 64 ? 0ull : (~0ull << lo));
+          vlo &= (uint32_t)range;
+          vhi &= (uint32_t)(range >> 32);
+        }
         float x[64];
         float tmax = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 64; ++e) {
           const uint32_t bits = e < 32 ? s0[e] : s1[e - 32];
-          const bool vis = e < nvis && (((e < 32 ? vlo : vhi) >> (e & 31)) & 1u);
+          const bool vis = ((e < 32 ? vlo : vhi) >> (e & 31)) & 1u;
           x[e] = vis ? __uint_as_float(bits) * p.scale_log2 : -INFINITY;
           tmax = fmaxf(tmax, x[e]);
         }

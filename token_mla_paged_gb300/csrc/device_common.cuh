@@ -104,16 +104,37 @@ __device__ __forceinline__ Item load_item(const DecodeParams& p, int idx) {
   if (p.causal) {
     // The group's last token sees the most; entries past its limit are masked for all rows.
     const int t_hi = (it.row0 + it.nrows - 1) / p.num_heads;
-    const int64_t lim = it.Lg - it.T + t_hi - it.base;
-    const int64_t count = lim < 0 ? 0 : lim / it.stride + 1;
+    const int64_t lim_abs = it.Lg - it.T + t_hi;
+    int64_t count;
+    if (p.kv_pos) {
+      // positions ascend within a request: count those <= the limit
+      int64_t lo = 0, hi = L;
+      while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)p.kv_pos[it.kv_off + mid] <= lim_abs) lo = mid + 1;
+        else hi = mid;
+      }
+      count = lo;
+    } else {
+      const int64_t lim = lim_abs - it.base;
+      count = lim < 0 ? 0 : lim / it.stride + 1;
+    }
     if ((int64_t)it.e1 > count) it.e1 = (int)(count > (int64_t)it.e0 ? count : (int64_t)it.e0);
   }
   return it;
 }
 
-// Causal visibility of local entry i for token t.
-__device__ __forceinline__ bool visible(const Item& it, int causal, int64_t i, int t) {
-  return !causal || it.base + i * it.stride <= it.Lg - it.T + t;
+// Global position of local entry i.
+__device__ __forceinline__ int64_t entry_pos(const Item& it, const DecodeParams& p, int64_t i) {
+  return p.kv_pos ? (int64_t)p.kv_pos[it.kv_off + i] : it.base + i * it.stride;
+}
+
+// Visibility of local entry i for token t: causal limit Lg - T + t and, with a
+// window W > 0, positions above limit - W.
+__device__ __forceinline__ bool visible(const Item& it, const DecodeParams& p, int64_t i, int t) {
+  if (!p.causal) return true;
+  const int64_t lim = it.Lg - it.T + t, g = entry_pos(it, p, i);
+  return g <= lim && (p.window <= 0 || g > lim - p.window);
 }
 
 }  // namespace mla

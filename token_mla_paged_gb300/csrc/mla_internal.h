@@ -88,6 +88,8 @@ struct DecodeParams {
   const int32_t* pos_base_per_req;
   const int32_t* g_kv_indptr;
   int32_t causal, pos_base, pos_stride;
+  const int32_t* kv_pos;  // nullable: per-entry global positions (ascending per request)
+  int32_t window;         // sliding window on causal rows, 0 = none
   int32_t batch, num_heads, max_q_len, num_workers, mode, items_cap;
   float scale_log2;      // softmax_scale * kappa * log2(e): logits in base 2
   float out_scale;       // kappa (fp8) or 1: applied to the PV accumulator

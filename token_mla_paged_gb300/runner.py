@@ -48,10 +48,11 @@ class DecodeRunner:
     def forward(self, *, q, kv_pool, kv_dtype: int, kv_indptr, kv_indices, qo_indptr, causal: bool,
                 softmax_scale: float, kv_scale: float, o, lse, pos_base: int = 0,
                 pos_stride: int = 1, pos_base_per_req=None, g_kv_indptr=None,
-                algo: int = MLA_ALGO_TENSOR, stream=None) -> None:
+                algo: int = MLA_ALGO_TENSOR, kv_pos=None, window: int = 0, stream=None) -> None:
         mla_decode_fwd(q=q, kv_pool=kv_pool, kv_dtype=kv_dtype, kv_indptr=kv_indptr,
                        kv_indices=kv_indices, qo_indptr=qo_indptr, causal=causal,
                        softmax_scale=softmax_scale, kv_scale=kv_scale, o=o, lse=lse,
                        params=self.params, plan_d=self.plan_d, workspace_d=self.workspace,
                        pos_base=pos_base, pos_stride=pos_stride, pos_base_per_req=pos_base_per_req,
-                       g_kv_indptr=g_kv_indptr, algo=algo, stream=stream)
+                       g_kv_indptr=g_kv_indptr, algo=algo, kv_pos=kv_pos, window=window,
+                       stream=stream)
