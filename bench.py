@@ -49,6 +49,13 @@ def build_workload(name: str):
         return mi.verify_fp8(), dict(mode=2, cap=0, shards=None)
     if name == "long_skewed_fp8":
         return mi.long_skewed_fp8(), dict(mode=1, cap=0, shards=None)
+    if name in ("csa_topk_fp8", "hca_fp8"):
+        # DSV4 layer types: 64 requests, 2 tokens (MTP), 128 heads, contexts 4k-64k
+        Lg = np.random.default_rng(mi.SEED_BASE + 8).integers(4096, 65537, size=64)
+        w = mi.sparse_variant("csa" if name.startswith("csa") else "hca", batch=64, num_heads=128,
+                              q_lens=[2] * 64, global_lens=Lg, window=128, topk=2048, ratio=128,
+                              kv_dtype="fp8")
+        return w, dict(mode=1, cap=0, shards=None)
     if name == "cp_shards_bf16":
         sw = mi.cp_shards_bf16()
         return sw.shards, dict(mode=1, cap=0, shards=sw)
@@ -66,9 +73,14 @@ def visible_pairs(w) -> int:
             continue
         base = int(w.pos_base_per_req[b]) if w.pos_base_per_req is not None else w.pos_base
         Lg = int(w.g_kv_indptr[b + 1] - w.g_kv_indptr[b]) if w.g_kv_indptr is not None else L
+        k0 = int(w.kv_indptr[b])
+        pos = (w.kv_pos[k0:k0 + L].astype(np.int64) if w.kv_pos is not None
+               else base + w.pos_stride * np.arange(L, dtype=np.int64))   # ascending either way
         for t in range(T):
-            lim = Lg - T + t - base
-            tot += 0 if lim < 0 else min(L, lim // w.pos_stride + 1)
+            lim = Lg - T + t
+            hi = int(np.searchsorted(pos, lim, side="right"))
+            lo = int(np.searchsorted(pos, lim - w.window, side="right")) if w.window > 0 else 0
+            tot += max(0, hi - lo)
     return tot * w.num_heads
 
 
@@ -76,7 +88,8 @@ def algorithmic_bytes(w) -> int:
     elem = 2 if w.kv_dtype == "bf16" else 1
     nnz = int(w.kv_indptr[-1] - w.kv_indptr[0])
     rows = w.total_q * w.num_heads
-    return nnz * 576 * elem + 4 * nnz + rows * (576 * 2 + 512 * 2 + 4)
+    pos_bytes = 4 * nnz if w.kv_pos is not None else 0
+    return nnz * 576 * elem + 4 * nnz + pos_bytes + rows * (576 * 2 + 512 * 2 + 4)
 
 
 def ncu_traffic(config: str, record: str = "ncu_traffic.json"):
@@ -214,6 +227,7 @@ def _single_request(w, b):
         w, kv_indptr=np.array([0, k1 - k0], np.int32), kv_indices=w.kv_indices[k0:k1],
         qo_indptr=np.array([0, q1 - q0], np.int32), q_bits=w.q_bits[q0:q1],
         pos_base_per_req=None if w.pos_base_per_req is None else w.pos_base_per_req[b:b + 1],
+        kv_pos=None if w.kv_pos is None else w.kv_pos[k0:k1],
         g_kv_indptr=None if w.g_kv_indptr is None else np.array(
             [0, int(w.g_kv_indptr[b + 1] - w.g_kv_indptr[b])], np.int32))
 
@@ -374,7 +388,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="draft_block_bf16", choices=mi.CONFIG_NAMES + mi.EXTRA_CONFIG_NAMES)
+    ap.add_argument("--config", default="draft_block_bf16",
+                    choices=mi.CONFIG_NAMES + mi.SPARSE_CONFIG_NAMES + mi.EXTRA_CONFIG_NAMES)
     ap.add_argument("--algo", default="tensor", choices=["tensor", "cuda_core"])
     ap.add_argument("--workers", type=int, default=0, help="plan workers (0 = kernel default)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

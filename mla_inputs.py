@@ -332,6 +332,8 @@ def sparse_variant(kind: str, *, batch: int, num_heads: int, q_lens, global_lens
                     window=window if kind == "swa" else 0)
 
 
+# decode over the DSV4 layer types' index lists (per-entry positions)
+SPARSE_CONFIG_NAMES = ["csa_topk_fp8", "hca_fp8"]
 # the KV-cache write that precedes the decode (a separate call, measured on its own)
 EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16"]
 
