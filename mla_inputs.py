@@ -332,6 +332,37 @@ def sparse_variant(kind: str, *, batch: int, num_heads: int, q_lens, global_lens
                     window=window if kind == "swa" else 0)
 
 
+@dataclasses.dataclass
+class RopeInputs:
+    """Inputs of the fused decode RoPE + q concat + cache write (bf16 bit patterns)."""
+    q_nope_bits: np.ndarray      # uint16 [n, H, 512] absorbed latent q
+    q_pe_bits: np.ndarray        # uint16 [n, H, 64] RoPE columns of q, not yet rotated
+    kv_c_bits: np.ndarray        # uint16 [n, 512]
+    k_pe_bits: np.ndarray        # uint16 [n, 64], not yet rotated
+    positions: np.ndarray        # int32 [n]
+    cos_sin: np.ndarray          # float32 [max_pos, 64]: cos of the 32 angles, then their sin
+    slot_mapping: np.ndarray     # int32 [n]
+    num_slots: int
+
+
+def rope_inputs(num_tokens: int, num_heads: int, max_pos: int = 131072, num_slots: Optional[int] = None,
+                seed: int = SEED_BASE + 9, rope_base: float = 10000.0) -> RopeInputs:
+    """Seeded activations N(0,1), positions uniform in [0, max_pos), slots a seeded
+    permutation prefix, and a rotary table for 32 angles p * base^(-2i/64) (the
+    plain RoPE table; models with scaled tables pass their own)."""
+    rng = np.random.default_rng(seed)
+    n, H = num_tokens, num_heads
+    if num_slots is None:
+        num_slots = max(16, _pow2_at_least(n))
+    f = lambda *shape: to_bf16_bits(rng.standard_normal(shape, dtype=np.float32))  # noqa: E731
+    inv_freq = rope_base ** (-np.arange(0, 64, 2, dtype=np.float64) / 64.0)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv_freq[None, :]
+    cos_sin = np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+    return RopeInputs(q_nope_bits=f(n, H, 512), q_pe_bits=f(n, H, 64), kv_c_bits=f(n, 512), k_pe_bits=f(n, 64),
+                      positions=rng.integers(0, max_pos, size=n).astype(np.int32), cos_sin=cos_sin,
+                      slot_mapping=rng.permutation(num_slots)[:n].astype(np.int32), num_slots=num_slots)
+
+
 # decode over the DSV4 layer types' index lists (per-entry positions)
 SPARSE_CONFIG_NAMES = ["csa_topk_fp8", "hca_fp8"]
 # the KV-cache write that precedes the decode (a separate call, measured on its own)
