@@ -380,6 +380,136 @@ def cache_write_main(args, rank: int, world: int):
         torch.distributed.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- fused RoPE + q concat + cache write
+
+RC_METRIC = "MLA fused decode RoPE + q concat + KV-cache write: tokens/s and achieved HBM GB/s on 1 GB300"
+RC_TOKENS, RC_HEADS, RC_SLOTS, RC_MAXPOS = 512, 128, 131072, 131072   # 64 requests x 8-token blocks
+
+
+def rope_cache_bytes(n: int, H: int) -> int:
+    """q_nope + q_pe read, q written (bf16), kv_c + k_pe read, fp8 row written,
+    position + slot, one 256-byte rotary row per token."""
+    return n * (H * (1024 + 128 + 1152) + 1152 + 576 + 8 + 256)
+
+
+def rope_cache_main(args, rank: int, world: int):
+    inp = mi.rope_inputs(RC_TOKENS, RC_HEADS, max_pos=RC_MAXPOS, num_slots=RC_SLOTS)
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        from oracle import rope_cache as rc
+        n = 64
+        pool = np.zeros((RC_SLOTS, 576), np.uint8)
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            rc.rope_q_cache(inp.q_nope_bits[:n], inp.q_pe_bits[:n], inp.kv_c_bits[:n], inp.k_pe_bits[:n],
+                            inp.positions[:n], inp.cos_sin, rc.NEOX, inp.slot_mapping[:n], pool, "fp8", 0.05)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        value = n * len(times) / sum(times)
+        print(json.dumps({"impl": "reference", "metric": RC_METRIC, "value": value, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                          "config": {"workload": args.config, "sample": f"{n} of {RC_TOKENS} tokens per step"},
+                          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                           "sample": f"{n} tokens per step"},
+                          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    import token_mla_paged_gb300 as m
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev_index = torch.cuda.current_device()
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q_nope, q_pe, kv_c, k_pe = bf(inp.q_nope_bits), bf(inp.q_pe_bits), bf(inp.kv_c_bits), bf(inp.k_pe_bits)
+    pos = torch.from_numpy(inp.positions).cuda()
+    cs = torch.from_numpy(inp.cos_sin).cuda()
+    slots = torch.from_numpy(inp.slot_mapping).cuda()
+    q_out = torch.empty(RC_TOKENS, RC_HEADS, 576, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(RC_SLOTS, 576, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        m.mla_rope_q_cache(q_nope, q_pe, q_out, kv_c, k_pe, pos, cs, slots, pool, m.MLA_KV_FP8_E4M3, 0.05)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world, device="cuda")
+    # end to end: the step's activations, positions and slots from pinned host memory,
+    # the fused call, and q read back (it is what the decode consumes next)
+    hosts = [t.cpu().pin_memory() for t in (q_nope, q_pe, kv_c, k_pe, pos, slots)]
+    devs = (q_nope, q_pe, kv_c, k_pe, pos, slots)
+    q_h = torch.empty_like(q_out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hosts)
+    d2h = q_h.numel() * q_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for d, h in zip(devs, hosts):
+            d.copy_(h, non_blocking=True)
+        step()
+        q_h.copy_(q_out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps, world, device="cuda")
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks = load_peaks()
+    nbytes = rope_cache_bytes(RC_TOKENS, RC_HEADS)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        from oracle import rope_cache as rc
+        n = 64
+        t0 = time.perf_counter()
+        rc.rope_q_cache(inp.q_nope_bits[:n], inp.q_pe_bits[:n], inp.kv_c_bits[:n], inp.k_pe_bits[:n],
+                        inp.positions[:n], inp.cos_sin, rc.NEOX, inp.slot_mapping[:n],
+                        np.zeros((RC_SLOTS, 576), np.uint8), "fp8", 0.05)
+        cpu = {"value": n / (time.perf_counter() - t0), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} of {RC_TOKENS} tokens"}
+    print(json.dumps({
+        "metric": RC_METRIC, "value": whole_job_rate(RC_TOKENS, world, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32-rope->fp8", "data": "synthetic",
+        "config": {"workload": args.config, "tokens": RC_TOKENS, "heads": RC_HEADS, "pool_slots": RC_SLOTS,
+                   "rope": "neox", "l2": "flushed (256 MB write) between timed steps"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic(args.config, "ncu_traffic_cache_write.json"),
+                     "peak_source": peaks["source"], "alg_bytes": nbytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": whole_job_rate(RC_TOKENS, world, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps, "clocks": clk.summary()}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -398,6 +528,8 @@ def main():
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.config == "rope_cache_fp8":
+        return rope_cache_main(args, rank, world)
     if args.config in mi.EXTRA_CONFIG_NAMES:
         return cache_write_main(args, rank, world)
 

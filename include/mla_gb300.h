@@ -261,6 +261,50 @@ typedef struct {
  * nothing is read back, so the call can be captured in a CUDA graph. */
 mla_status mla_cache_write(const mla_cache_write_args* args, void* stream);
 
+/* Rotation layout of the 64 RoPE columns: neox pairs column i with i + 32,
+ * interleaved pairs columns 2i and 2i + 1. */
+typedef enum { MLA_ROPE_NEOX = 0, MLA_ROPE_INTERLEAVED = 1 } mla_rope_style;
+
+/* Arguments of the fused decode RoPE + q concat + cache write.  Device pointers;
+ * every activation is bf16 with 16-byte aligned rows (strides in elements,
+ * multiples of 8). */
+typedef struct {
+  const void* q_nope;              /* [n, H, 512] absorbed latent q */
+  int64_t q_nope_stride_token, q_nope_stride_head;
+  const void* q_pe;                /* [n, H, 64] RoPE columns of q, not yet rotated */
+  int64_t q_pe_stride_token, q_pe_stride_head;
+  void* q_out;                     /* [n, H, 576] bf16, contiguous: the q mla_decode_fwd reads */
+  int32_t num_heads;               /* H >= 1 */
+  int32_t rope_style;              /* mla_rope_style */
+  const void* kv_c;                /* [n, 512] */
+  int64_t kv_c_stride;             /* >= 512 */
+  const void* k_pe;                /* [n, 64], not yet rotated */
+  int64_t k_pe_stride;             /* >= 64 */
+  const int32_t* positions;        /* [n] position of each token; outside [0, max_pos) clamps */
+  const float* cos_sin;            /* fp32 [max_pos, 64]: cos of the 32 angles, then their sin */
+  int64_t max_pos;                 /* >= 1 */
+  const int32_t* slot_mapping;     /* [n] pool slot; < 0 or >= num_slots: no cache write */
+  int64_t num_tokens;              /* n >= 0 */
+  void* kv_pool;                   /* bf16 | fp8 [num_slots, 576] */
+  int64_t num_slots;
+  int32_t kv_dtype;                /* mla_kv_dtype */
+  float kv_scale;                  /* fp8: finite, > 0 */
+} mla_rope_q_cache_args;
+
+/* Fused decode RoPE + q concat + KV-cache write, the step after the absorb and
+ * before the decode ("[ROCm] Dspark MLA module": fused_qk_rope_concat_and_cache_mla,
+ * decode RoPE + cache after absorb, a follow-up there).  For token n at position
+ * p (clamped), with c = cos_sin[p, 0:32], s = cos_sin[p, 32:64] and the 64 RoPE
+ * values split into pairs (a, b) by rope_style:
+ *   rotated pair = (a*c - b*s, b*c + a*s), every product and sum rounded to
+ *   float32 on its own (no fused multiply-add);
+ *   q_out[n, h] = (q_nope[n, h, 0:512], bf16(rotated q_pe[n, h]));
+ *   pool[slot_mapping[n]] = the mla_cache_write row of (kv_c[n], rotated k_pe[n]).
+ * The rotation runs in float32 and its result is converted for the cache, never
+ * reinterpreted (the same page shows a float32 rotated k_pe read as bf16).
+ * Enqueued on `stream`; graph-capturable. */
+mla_status mla_rope_q_cache(const mla_rope_q_cache_args* args, void* stream);
+
 /* Forward call for callers that cannot allocate device memory (a runtime or
  * allocator that hands out only input and output tensors): the plan buffer and
  * the workspace come from one static device array of 16 MiB inside the library

@@ -366,7 +366,7 @@ def rope_inputs(num_tokens: int, num_heads: int, max_pos: int = 131072, num_slot
 # decode over the DSV4 layer types' index lists (per-entry positions)
 SPARSE_CONFIG_NAMES = ["csa_topk_fp8", "hca_fp8"]
 # the KV-cache write that precedes the decode (a separate call, measured on its own)
-EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16"]
+EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16", "rope_cache_fp8"]
 
 
 @dataclasses.dataclass

@@ -194,3 +194,32 @@ def test_cache_write_rejects_bad_arguments_before_touching_the_device():
     assert lib.mla_cache_write(args(num_tokens=4, k_pe=0x20008), None) == 1
     assert lib.mla_cache_write(args(num_tokens=4, kv_c_stride=516), None) == 1
     assert lib.mla_cache_write(args(num_tokens=4, k_pe_dtype=m.MLA_ACT_FP32, k_pe_stride=66), None) == 1
+
+
+def test_rope_q_cache_rejects_bad_arguments_before_touching_the_device():
+    import ctypes
+    lib = m.library()
+
+    def args(**kw):
+        a = m.RopeArgs()
+        a.q_nope, a.q_nope_stride_token, a.q_nope_stride_head = 0x10000, 1024, 512
+        a.q_pe, a.q_pe_stride_token, a.q_pe_stride_head = 0x20000, 128, 64
+        a.q_out, a.num_heads, a.rope_style = 0x30000, 2, m.MLA_ROPE_NEOX
+        a.kv_c, a.kv_c_stride, a.k_pe, a.k_pe_stride = 0x40000, 512, 0x50000, 64
+        a.positions, a.cos_sin, a.max_pos = 0x60000, 0x70000, 128
+        a.slot_mapping, a.num_tokens = 0x80000, 0
+        a.kv_pool, a.num_slots, a.kv_dtype, a.kv_scale = 0x90000, 16, m.MLA_KV_FP8_E4M3, 0.05
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return ctypes.byref(a)
+
+    assert lib.mla_rope_q_cache(args(), None) == 0                      # nothing to do
+    assert lib.mla_rope_q_cache(None, None) == 1
+    assert lib.mla_rope_q_cache(args(rope_style=2), None) == 1
+    assert lib.mla_rope_q_cache(args(num_heads=0), None) == 1
+    assert lib.mla_rope_q_cache(args(max_pos=0), None) == 1
+    assert lib.mla_rope_q_cache(args(kv_scale=-1.0), None) == 1
+    assert lib.mla_rope_q_cache(args(kv_dtype=5), None) == 1
+    assert lib.mla_rope_q_cache(args(num_tokens=3, q_out=None), None) == 1
+    assert lib.mla_rope_q_cache(args(num_tokens=3, q_pe_stride_head=68), None) == 1   # not 16-byte rows
+    assert lib.mla_rope_q_cache(args(num_tokens=3, kv_c=0x40008), None) == 1          # misaligned

@@ -24,6 +24,7 @@ MLA_OUT_BF16, MLA_OUT_FP32 = 0, 1
 MLA_PLAN_STATIC, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST = 0, 1, 2
 MLA_ALGO_TENSOR, MLA_ALGO_CUDA_CORE = 0, 1
 MLA_ACT_BF16, MLA_ACT_FP32 = 0, 1
+MLA_ROPE_NEOX, MLA_ROPE_INTERLEAVED = 0, 1
 D_QK, D_V = 576, 512
 
 DEVICE_ERRORS = {0: "ok", 1: "kv index out of range", 2: "decreasing indptr",
@@ -67,6 +68,18 @@ class CacheWriteArgs(ctypes.Structure):
                 ("kv_scale", ctypes.c_float)]
 
 
+class RopeArgs(ctypes.Structure):
+    _fields_ = [("q_nope", ctypes.c_void_p), ("q_nope_stride_token", ctypes.c_int64),
+                ("q_nope_stride_head", ctypes.c_int64), ("q_pe", ctypes.c_void_p),
+                ("q_pe_stride_token", ctypes.c_int64), ("q_pe_stride_head", ctypes.c_int64),
+                ("q_out", ctypes.c_void_p), ("num_heads", ctypes.c_int32), ("rope_style", ctypes.c_int32),
+                ("kv_c", ctypes.c_void_p), ("kv_c_stride", ctypes.c_int64), ("k_pe", ctypes.c_void_p),
+                ("k_pe_stride", ctypes.c_int64), ("positions", ctypes.c_void_p), ("cos_sin", ctypes.c_void_p),
+                ("max_pos", ctypes.c_int64), ("slot_mapping", ctypes.c_void_p), ("num_tokens", ctypes.c_int64),
+                ("kv_pool", ctypes.c_void_p), ("num_slots", ctypes.c_int64), ("kv_dtype", ctypes.c_int32),
+                ("kv_scale", ctypes.c_float)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; "
@@ -84,6 +97,7 @@ def _load():
         "mla_decode_fwd_noalloc": (ctypes.c_int, [ctypes.POINTER(FwdArgs), vp]),
         "mla_merge_states": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, i32, vp, vp]),
         "mla_cache_write": (ctypes.c_int, [ctypes.POINTER(CacheWriteArgs), vp]),
+        "mla_rope_q_cache": (ctypes.c_int, [ctypes.POINTER(RopeArgs), vp]),
         "mla_get_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
@@ -98,7 +112,7 @@ _lib = _load()
 # Symbols the header declares; tests check the library exports each one.
 ABI_SYMBOLS = ("mla_abi_version", "mla_status_string", "mla_decode_plan_size", "mla_decode_plan",
                "mla_decode_plan_device", "mla_decode_fwd", "mla_merge_states",
-               "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write")
+               "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write", "mla_rope_q_cache")
 
 
 def library():
@@ -244,6 +258,30 @@ def mla_cache_write(kv_c, k_pe, slot_mapping, kv_pool, kv_dtype: int, kv_scale: 
     a.kv_dtype = kv_dtype
     a.kv_scale = kv_scale
     _check(_lib.mla_cache_write(ctypes.byref(a), _stream(stream)), "mla_cache_write")
+
+
+def mla_rope_q_cache(q_nope, q_pe, q_out, kv_c, k_pe, positions, cos_sin, slot_mapping, kv_pool,
+                     kv_dtype: int, kv_scale: float = 1.0, rope_style: int = MLA_ROPE_NEOX,
+                     stream=None) -> None:
+    """q_nope [n, H, 512], q_pe [n, H, 64], kv_c [n, 512], k_pe [n, 64] (bf16, unit
+    stride along the row); q_out bf16 [n, H, 576] contiguous; positions and
+    slot_mapping int32 [n]; cos_sin fp32 [max_pos, 64]; kv_pool [slots, 576]."""
+    import torch
+    for t in (q_nope, q_pe, kv_c, k_pe, q_out):
+        if t.dtype != torch.bfloat16 or t.stride(-1) != 1:
+            raise MlaError(1, "mla_rope_q_cache: activations must be bf16 with unit stride along the row")
+    if not q_out.is_contiguous() or cos_sin.dtype != torch.float32 or not cos_sin.is_contiguous():
+        raise MlaError(1, "mla_rope_q_cache: q_out must be contiguous and cos_sin contiguous fp32")
+    a = RopeArgs()
+    a.q_nope, a.q_nope_stride_token, a.q_nope_stride_head = _ptr(q_nope), q_nope.stride(0), q_nope.stride(1)
+    a.q_pe, a.q_pe_stride_token, a.q_pe_stride_head = _ptr(q_pe), q_pe.stride(0), q_pe.stride(1)
+    a.q_out, a.num_heads, a.rope_style = _ptr(q_out), int(q_nope.shape[1]), rope_style
+    a.kv_c, a.kv_c_stride = _ptr(kv_c), kv_c.stride(0)
+    a.k_pe, a.k_pe_stride = _ptr(k_pe), k_pe.stride(0)
+    a.positions, a.cos_sin, a.max_pos = _ptr(positions), _ptr(cos_sin), int(cos_sin.shape[0])
+    a.slot_mapping, a.num_tokens = _ptr(slot_mapping), int(slot_mapping.shape[0])
+    a.kv_pool, a.num_slots, a.kv_dtype, a.kv_scale = _ptr(kv_pool), int(kv_pool.shape[0]), kv_dtype, kv_scale
+    _check(_lib.mla_rope_q_cache(ctypes.byref(a), _stream(stream)), "mla_rope_q_cache")
 
 
 def mla_get_device_error(workspace_d, stream=None) -> Tuple[int, int]:

@@ -191,6 +191,29 @@ mla_status mla_cache_write(const mla_cache_write_args* a, void* stream) {
   return launch_cache_write(*a, stream);
 }
 
+mla_status mla_rope_q_cache(const mla_rope_q_cache_args* a, void* stream) {
+  if (!a) return MLA_ERR_INVALID_ARG;
+  if (a->num_heads < 1 || a->num_tokens < 0 || a->max_pos < 1 || a->num_slots <= 0) return MLA_ERR_INVALID_ARG;
+  if (a->rope_style != MLA_ROPE_NEOX && a->rope_style != MLA_ROPE_INTERLEAVED) return MLA_ERR_INVALID_ARG;
+  if (a->kv_dtype != MLA_KV_BF16 && a->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (a->kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(a->kv_scale) && a->kv_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (a->kv_c_stride < 512 || a->k_pe_stride < 64) return MLA_ERR_INVALID_ARG;
+  if (a->num_tokens == 0) return MLA_OK;
+  if (!a->q_nope || !a->q_pe || !a->q_out || !a->kv_c || !a->k_pe || !a->positions || !a->cos_sin ||
+      !a->slot_mapping || !a->kv_pool)
+    return MLA_ERR_INVALID_ARG;
+  const int64_t strides[] = {a->q_nope_stride_token, a->q_nope_stride_head, a->q_pe_stride_token,
+                             a->q_pe_stride_head, a->kv_c_stride, a->k_pe_stride};
+  for (int64_t st : strides)
+    if (st < 0 || st % 8 != 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned(a->q_nope, 16) || !aligned(a->q_pe, 16) || !aligned(a->q_out, 16) || !aligned(a->kv_c, 16) ||
+      !aligned(a->k_pe, 16) || !aligned(a->kv_pool, 16) || !aligned(a->cos_sin, 4) ||
+      !aligned(a->positions, 4) || !aligned(a->slot_mapping, 4))
+    return MLA_ERR_INVALID_ARG;
+  return launch_rope_q_cache(*a, stream);
+}
+
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info) {
   if (!workspace_d || !code) return MLA_ERR_INVALID_ARG;
   int32_t h[2] = {0, 0};

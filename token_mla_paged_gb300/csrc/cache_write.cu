@@ -135,6 +135,118 @@ __global__ void __launch_bounds__(256, (kF32C || kF32PE) ? 2 : 4) mla_cache_writ
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode RoPE + q concat + cache write ("[ROCm] Dspark MLA module":
+// fused_qk_rope_concat_and_cache_mla, decode RoPE + cache after absorb).
+
+struct RopeParams {
+  const uint16_t* q_nope;
+  int64_t qn_tok, qn_head;               // element strides
+  const uint16_t* q_pe;
+  int64_t qp_tok, qp_head;
+  uint16_t* q_out;                       // [n, H, 576]
+  int num_heads;
+  const uint16_t* kv_c;
+  int64_t kv_c_stride;
+  const uint16_t* k_pe;
+  int64_t k_pe_stride;
+  const int32_t* positions;
+  const float* cos_sin;                  // [max_pos, 64]
+  int64_t max_pos;
+  int style;                             // MLA_ROPE_NEOX | MLA_ROPE_INTERLEAVED
+  const int32_t* slot_mapping;
+  int64_t num_tokens, num_slots;
+  void* pool;
+  float inv_scale;
+};
+
+// y_a = a*c - b*s, y_b = b*c + a*s, every product and sum rounded on its own.
+__device__ __forceinline__ void rot(float a, float b, float c, float sn, float& ya, float& yb) {
+  ya = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, sn));
+  yb = __fadd_rn(__fmul_rn(b, c), __fmul_rn(a, sn));
+}
+
+__device__ __forceinline__ void widen_bf16x8(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = __uint_as_float(w[k] << 16);
+    v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&v)[8]) {
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
+// Rotate the 64 RoPE values held as 16-byte units (8 values each) by the lanes
+// that own them.  neox: lane l < 4 owns units l and l + 4 (values 8l.. and
+// 32 + 8l.., the halves that pair up); interleaved: lane l < 8 owns unit l
+// (four adjacent pairs).  Unit k of the rotated row is written to out(k).
+template <typename Out>
+__device__ __forceinline__ void rope_row(const uint16_t* src, int lane, int style, const float* cs, Out out) {
+  if (style == MLA_ROPE_NEOX) {
+    if (lane < 4) {
+      float a[8], b[8], ya[8], yb[8];
+      widen_bf16x8(__ldg(reinterpret_cast<const uint4*>(src) + lane), a);
+      widen_bf16x8(__ldg(reinterpret_cast<const uint4*>(src) + lane + 4), b);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) rot(a[k], b[k], __ldg(cs + 8 * lane + k), __ldg(cs + 32 + 8 * lane + k), ya[k], yb[k]);
+      out(lane, ya);
+      out(lane + 4, yb);
+    }
+  } else {
+    if (lane < 8) {
+      float x[8], y[8];
+      widen_bf16x8(__ldg(reinterpret_cast<const uint4*>(src) + lane), x);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        rot(x[2 * k], x[2 * k + 1], __ldg(cs + 4 * lane + k), __ldg(cs + 32 + 4 * lane + k), y[2 * k], y[2 * k + 1]);
+      out(lane, y);
+    }
+  }
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(256) mla_rope_q_cache_kernel(const RopeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nq = p.num_tokens * p.num_heads;
+  const int64_t items = nq + p.num_tokens;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t it = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += warps) {
+    const int64_t n = it < nq ? it / p.num_heads : it - nq;
+    int64_t pos = __ldg(p.positions + n);
+    pos = pos < 0 ? 0 : (pos >= p.max_pos ? p.max_pos - 1 : pos);   // outside the table: clamp
+    const float* cs = p.cos_sin + pos * 64;
+    if (it < nq) {
+      // q row: 512 absorbed latent columns copied, 64 RoPE columns rotated, one 576-wide row
+      const int h = (int)(it - n * p.num_heads);
+      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + n * p.qn_tok + h * p.qn_head);
+      uint4* qo = reinterpret_cast<uint4*>(p.q_out + (n * p.num_heads + h) * kDqk);
+      const uint4 u0 = __ldg(qn + lane), u1 = __ldg(qn + lane + 32);
+      qo[lane] = u0;
+      qo[lane + 32] = u1;
+      rope_row(p.q_pe + n * p.qp_tok + h * p.qp_head, lane, p.style, cs,
+                  [&](int k, const float (&v)[8]) { qo[64 + k] = pack_bf16x8(v); });
+    } else {
+      // cache row: kv_c and the rotated k_pe, encoded like mla_cache_write
+      const int32_t slot = __ldg(p.slot_mapping + n);
+      if (slot < 0 || slot >= p.num_slots) continue;
+      CacheWriteParams cw;
+      cw.pool = p.pool;
+      cw.inv_scale = p.inv_scale;
+      const uint4* kc = reinterpret_cast<const uint4*>(p.kv_c + n * p.kv_c_stride);
+      float f[8];
+      widen_bf16x8(__ldg(kc + lane), f);
+      store8<kFp8>(cw, slot, lane, f);
+      widen_bf16x8(__ldg(kc + lane + 32), f);
+      store8<kFp8>(cw, slot, lane + 32, f);
+      rope_row(p.k_pe + n * p.k_pe_stride, lane, p.style, cs,
+                     [&](int k, const float (&v)[8]) { store8<kFp8>(cw, slot, kGroupsC + k, v); });
+    }
+  }
+}
+
 }  // namespace
 
 mla_status launch_cache_write(const mla_cache_write_args& a, void* stream) {
@@ -168,6 +280,44 @@ mla_status launch_cache_write(const mla_cache_write_args& a, void* stream) {
       mla_cache_write_kernel<true, false, false>,  mla_cache_write_kernel<true, false, true>,
       mla_cache_write_kernel<true, true, false>,   mla_cache_write_kernel<true, true, true>};
   kernels[sel]<<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status launch_rope_q_cache(const mla_rope_q_cache_args& a, void* stream) {
+  RopeParams p;
+  p.q_nope = static_cast<const uint16_t*>(a.q_nope);
+  p.qn_tok = a.q_nope_stride_token;
+  p.qn_head = a.q_nope_stride_head;
+  p.q_pe = static_cast<const uint16_t*>(a.q_pe);
+  p.qp_tok = a.q_pe_stride_token;
+  p.qp_head = a.q_pe_stride_head;
+  p.q_out = static_cast<uint16_t*>(a.q_out);
+  p.num_heads = a.num_heads;
+  p.kv_c = static_cast<const uint16_t*>(a.kv_c);
+  p.kv_c_stride = a.kv_c_stride;
+  p.k_pe = static_cast<const uint16_t*>(a.k_pe);
+  p.k_pe_stride = a.k_pe_stride;
+  p.positions = a.positions;
+  p.cos_sin = a.cos_sin;
+  p.max_pos = a.max_pos;
+  p.style = a.rope_style;
+  p.slot_mapping = a.slot_mapping;
+  p.num_tokens = a.num_tokens;
+  p.num_slots = a.num_slots;
+  p.pool = a.kv_pool;
+  const bool fp8 = a.kv_dtype == MLA_KV_FP8_E4M3;
+  p.inv_scale = fp8 ? 1.0f / a.kv_scale : 1.0f;
+  if (a.num_tokens == 0) return MLA_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const int64_t items = a.num_tokens * ((int64_t)a.num_heads + 1);
+  const int64_t blocks_needed = (items + 7) / 8;
+  const int64_t cap = (int64_t)sms * 8;
+  const int blocks = (int)(blocks_needed < cap ? blocks_needed : cap);
+  if (fp8) mla_rope_q_cache_kernel<true><<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
+  else mla_rope_q_cache_kernel<false><<<blocks, 256, 0, (cudaStream_t)stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
