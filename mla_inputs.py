@@ -363,10 +363,35 @@ def rope_inputs(num_tokens: int, num_heads: int, max_pos: int = 131072, num_slot
                       slot_mapping=rng.permutation(num_slots)[:n].astype(np.int32), num_slots=num_slots)
 
 
+@dataclasses.dataclass
+class BmmInputs:
+    """One absorb BMM: activations x (bf16 bits [n, H, K]) times a per-head weight
+    stored as [H, K, N] (bf16 bits, or fp8 e4m3fn codes with a per-tensor scale)."""
+    x_bits: np.ndarray
+    w_bits: np.ndarray
+    w_dtype: str
+    w_scale: float
+
+
+def bmm_inputs(num_tokens: int, num_heads: int, k: int, n: int, w_dtype: str = "fp8",
+               seed: int = SEED_BASE + 11, x_std: float = 1.0) -> BmmInputs:
+    """Seeded x ~ N(0, x_std^2) and weights ~ N(0, 1/k) (unit-scale outputs, the
+    usual initialisation of a projection); an fp8 weight is stored per tensor as
+    e4m3fn(w / s) with s = max|w| / 448.  Absorb: k=128, n=512 (W_UK); un-absorb:
+    k=512, n=128 (W_UV)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((num_tokens, num_heads, k), dtype=np.float32) * np.float32(x_std)
+    w = rng.standard_normal((num_heads, k, n), dtype=np.float32) * np.float32(1.0 / math.sqrt(k))
+    if w_dtype == "bf16":
+        return BmmInputs(to_bf16_bits(x), to_bf16_bits(w), "bf16", 1.0)
+    scale = float(np.float32(np.abs(w).max() / 448.0))
+    return BmmInputs(to_bf16_bits(x), to_fp8_bits(w, scale), "fp8", scale)
+
+
 # decode over the DSV4 layer types' index lists (per-entry positions)
 SPARSE_CONFIG_NAMES = ["csa_topk_fp8", "hca_fp8"]
 # the KV-cache write that precedes the decode (a separate call, measured on its own)
-EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16", "rope_cache_fp8"]
+EXTRA_CONFIG_NAMES = ["cache_write_fp8", "cache_write_bf16", "rope_cache_fp8", "absorb_bmm_fp8"]
 
 
 @dataclasses.dataclass
