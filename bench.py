@@ -510,6 +510,152 @@ def rope_cache_main(args, rank: int, world: int):
         torch.distributed.destroy_process_group()
 
 
+AB_METRIC = "MLA absorb + un-absorb BMMs (fp8 weights): tokens/s and achieved HBM GB/s on 1 GB300"
+AB_TOKENS, AB_HEADS = 256, 128          # 32 requests x 8-token blocks, 128 local heads
+
+
+def absorb_bytes(n: int, H: int, k: int, n_out: int, w_bytes: int = 1) -> int:
+    """Activations read (bf16), the weight read once, the result written (bf16)."""
+    return n * H * k * 2 + H * k * n_out * w_bytes + n * H * n_out * 2
+
+
+def absorb_main(args, rank: int, world: int):
+    wk = mi.bmm_inputs(AB_TOKENS, AB_HEADS, 128, 512, "fp8", seed=mi.SEED_BASE + 11)
+    wv = mi.bmm_inputs(AB_TOKENS, AB_HEADS, 512, 128, "fp8", seed=mi.SEED_BASE + 12)
+    sample = 32
+
+    def oracle_step(n):
+        from oracle import absorb_bmm as ab
+        ab.absorb_bmm(wk.x_bits[:n], wk.w_bits, "fp8", wk.w_scale)
+        ab.absorb_bmm(wv.x_bits[:n], wv.w_bits, "fp8", wv.w_scale)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        times = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle_step(sample)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        value = sample * len(times) / sum(times)
+        print(json.dumps({"impl": "reference", "metric": AB_METRIC, "value": value, "unit": "tokens/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": args.config, "sample": f"{sample} of {AB_TOKENS} tokens per step"},
+                          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1,
+                                           "kind": "oracle", "sample": f"{sample} tokens per step"},
+                          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}))
+        return
+    import torch
+    import token_mla_paged_gb300 as m
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev_index = torch.cuda.current_device()
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q_nope, o_lat = bf(wk.x_bits), bf(wv.x_bits)
+    w_uk = torch.from_numpy(wk.w_bits).cuda()
+    w_uv = torch.from_numpy(wv.w_bits).cuda()
+    q = torch.zeros(AB_TOKENS, AB_HEADS, 576, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(AB_TOKENS, AB_HEADS, 128, dtype=torch.bfloat16, device="cuda")
+    q_lat = q[..., :512]
+    stream = torch.cuda.current_stream()
+
+    def absorb():
+        m.mla_absorb_bmm(q_nope, w_uk, q_lat, wk.w_scale)
+
+    def unabsorb():
+        m.mla_absorb_bmm(o_lat, w_uv, out, wv.w_scale)
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        absorb()
+        unabsorb()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            absorb()
+            ev[i][1].record(stream)
+            unabsorb()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_a = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
+    ms_u = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
+    ms = slowest_rank_ms(ms_a + ms_u, world, device="cuda")
+    # end to end: q_nope and the decode output from pinned host memory, both BMMs,
+    # the 576-wide q and the un-absorbed output read back
+    hosts = [t.cpu().pin_memory() for t in (q_nope, o_lat)]
+    devs = (q_nope, o_lat)
+    q_h = torch.empty_like(q, device="cpu").pin_memory()
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hosts)
+    d2h = q_h.numel() * q_h.element_size() + out_h.numel() * out_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        for d, h in zip(devs, hosts):
+            d.copy_(h, non_blocking=True)
+        absorb()
+        unabsorb()
+        q_h.copy_(q, non_blocking=True)
+        out_h.copy_(out, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps, world, device="cuda")
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peaks = load_peaks()
+    b_a = absorb_bytes(AB_TOKENS, AB_HEADS, 128, 512)
+    b_u = absorb_bytes(AB_TOKENS, AB_HEADS, 512, 128)
+    dominant = "absorb" if ms_a >= ms_u else "unabsorb"
+    nbytes, ms_dom = (b_a, ms_a) if dominant == "absorb" else (b_u, ms_u)
+    gbs = nbytes / (ms_dom * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        t0 = time.perf_counter()
+        oracle_step(sample)
+        cpu = {"value": sample / (time.perf_counter() - t0), "unit": "tokens/s", "cores": 1,
+               "kind": "oracle", "sample": f"{sample} of {AB_TOKENS} tokens, both BMMs"}
+    key = args.config if dominant == "absorb" else args.config + "/unabsorb"
+    print(json.dumps({
+        "metric": AB_METRIC, "value": whole_job_rate(AB_TOKENS, world, ms), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x e4m3 -> f32", "data": "synthetic",
+        "config": {"workload": args.config, "tokens": AB_TOKENS, "heads": AB_HEADS,
+                   "absorb": "q_nope[256,128,128] @ W_UK[128,128,512] -> q[..., :512]",
+                   "unabsorb": "o_lat[256,128,512] @ W_UV[128,512,128]",
+                   "l2": "flushed (256 MB write) between timed steps"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic(key, "ncu_traffic_absorb_bmm.json"),
+                     "peak_source": peaks["source"], "alg_bytes": nbytes, "kernel": f"mla_absorb_bmm ({dominant})",
+                     "absorb_us": 1e3 * ms_a, "unabsorb_us": 1e3 * ms_u,
+                     "absorb_gbs": b_a / (ms_a * 1e-3) / 1e9, "unabsorb_gbs": b_u / (ms_u * 1e-3) / 1e9},
+        "cpu_baseline": cpu,
+        "e2e": {"value": whole_job_rate(AB_TOKENS, world, e2e_ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps, "clocks": clk.summary()}))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -530,6 +676,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.config == "rope_cache_fp8":
         return rope_cache_main(args, rank, world)
+    if args.config == "absorb_bmm_fp8":
+        return absorb_main(args, rank, world)
     if args.config in mi.EXTRA_CONFIG_NAMES:
         return cache_write_main(args, rank, world)
 

@@ -68,7 +68,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 3
+#define MLA_ABI_VERSION 4
 #define MLA_D_QK 576             /* latent 512 + RoPE 64 */
 #define MLA_D_V 512
 #define MLA_ROWS_PER_GROUP 128   /* query rows (t,h) handled together */
@@ -177,7 +177,9 @@ typedef struct {
 } mla_fwd_args;
 
 /* ABI version (MLA_ABI_VERSION); lets a caller probe capabilities by number
- * rather than by inspecting signatures. */
+ * rather than by inspecting signatures.  3: per-entry positions and the sliding
+ * window in mla_fwd_args, HOST plans, mla_cache_write, mla_rope_q_cache;
+ * 4: mla_absorb_bmm. */
 int mla_abi_version(void);
 
 /* Static description of a status code; never NULL. */
@@ -304,6 +306,40 @@ typedef struct {
  * reinterpreted (the same page shows a float32 rotated k_pe read as bf16).
  * Enqueued on `stream`; graph-capturable. */
 mla_status mla_rope_q_cache(const mla_rope_q_cache_args* args, void* stream);
+
+/* Storage type of an absorb BMM weight. */
+typedef enum { MLA_W_BF16 = 0, MLA_W_FP8_E4M3 = 1 } mla_weight_dtype;
+
+/* Arguments of one absorb BMM.  Device pointers; strides in elements. */
+typedef struct {
+  const void* x;                /* bf16 [num_tokens, num_heads, k], unit stride along k */
+  int64_t x_stride_token, x_stride_head;
+  const void* w;                /* [num_heads, k, n] contiguous (n fastest): torch.bmm's right operand */
+  int32_t w_dtype;              /* mla_weight_dtype */
+  float w_scale;                /* per-tensor scale applied to the product; finite (1 for plain bf16) */
+  void* out;                    /* bf16 [num_tokens, num_heads, n], unit stride along n */
+  int64_t out_stride_token, out_stride_head;
+  int32_t num_tokens;           /* >= 0 */
+  int32_t num_heads;            /* 1 .. 65535 */
+  int32_t k;                    /* multiple of 64, 64 .. 8192 */
+  int32_t n;                    /* multiple of 128, 128 .. 8192 */
+  int32_t* status_d;            /* optional device int32[2]: a bounded wait that runs out writes
+                                   (MLA_DEV_WAIT_TIMEOUT, site); NULL = not recorded */
+} mla_absorb_bmm_args;
+
+/* The absorb BMMs either side of the latent decode ("[ROCm] Dspark MLA module",
+ * Details: the decode's absorb BMM, an FP8/FP4 BMM when enabled, else torch.bmm):
+ * before it q_lat = q_nope @ W_UK per head (k = 128, n = 512), after it
+ * out = o_lat @ W_UV per head (k = 512, n = 128).  For every token t and head h:
+ *   out[t, h, j] = bf16( w_scale * sum_k x[t, h, k] * w[h, k, j] )
+ * with an fp8 weight decoded exactly (e4m3fn), products exact and summed in
+ * float32 on the tensor cores, the float32 sum times w_scale rounded to bf16
+ * (nearest, ties to even).  out may be a column slice of a wider buffer (e.g. the
+ * first 512 columns of the 576-wide q) through its strides.  Pointers 16-byte
+ * aligned and strides multiples of 8, x_stride_head >= k, out_stride_head >= n,
+ * else MLA_ERR_INVALID_ARG.  Enqueued on `stream`; nothing is read back, so the
+ * call can be captured in a CUDA graph. */
+mla_status mla_absorb_bmm(const mla_absorb_bmm_args* args, void* stream);
 
 /* Forward call for callers that cannot allocate device memory (a runtime or
  * allocator that hands out only input and output tensors): the plan buffer and

@@ -223,3 +223,34 @@ def test_rope_q_cache_rejects_bad_arguments_before_touching_the_device():
     assert lib.mla_rope_q_cache(args(num_tokens=3, q_out=None), None) == 1
     assert lib.mla_rope_q_cache(args(num_tokens=3, q_pe_stride_head=68), None) == 1   # not 16-byte rows
     assert lib.mla_rope_q_cache(args(num_tokens=3, kv_c=0x40008), None) == 1          # misaligned
+
+
+def test_absorb_bmm_rejects_bad_arguments_before_touching_the_device():
+    import ctypes
+    lib = m.library()
+
+    def args(**kw):
+        a = m.BmmArgs()
+        a.x, a.x_stride_token, a.x_stride_head = 0x10000, 4 * 128, 128
+        a.w, a.w_dtype, a.w_scale = 0x20000, m.MLA_W_FP8_E4M3, 0.01
+        a.out, a.out_stride_token, a.out_stride_head = 0x30000, 4 * 576, 576
+        a.num_tokens, a.num_heads, a.k, a.n = 0, 4, 128, 512
+        a.status_d = None
+        for k, v in kw.items():
+            setattr(a, k, v)
+        return ctypes.byref(a)
+
+    assert lib.mla_absorb_bmm(args(), None) == 0                         # nothing to do
+    assert lib.mla_absorb_bmm(None, None) == 1
+    assert lib.mla_absorb_bmm(args(k=96), None) == 1                     # k not a multiple of 64
+    assert lib.mla_absorb_bmm(args(n=192), None) == 1                    # n not a multiple of 128
+    assert lib.mla_absorb_bmm(args(num_heads=0), None) == 1
+    assert lib.mla_absorb_bmm(args(num_heads=70000), None) == 1
+    assert lib.mla_absorb_bmm(args(w_dtype=2), None) == 1
+    assert lib.mla_absorb_bmm(args(w_scale=float("nan")), None) == 1
+    assert lib.mla_absorb_bmm(args(x_stride_head=64), None) == 1         # rows overlap
+    assert lib.mla_absorb_bmm(args(out_stride_head=500), None) == 1
+    assert lib.mla_absorb_bmm(args(num_tokens=3, out_stride_token=4 * 576 + 4), None) == 1  # not 16-byte rows
+    assert lib.mla_absorb_bmm(args(num_tokens=3, w=None), None) == 1
+    assert lib.mla_absorb_bmm(args(num_tokens=3, x=0x10008), None) == 1  # misaligned
+    assert lib.mla_absorb_bmm(args(num_tokens=3, status_d=0x40002), None) == 1

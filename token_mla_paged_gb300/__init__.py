@@ -25,6 +25,7 @@ MLA_PLAN_STATIC, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST = 0, 1, 2
 MLA_ALGO_TENSOR, MLA_ALGO_CUDA_CORE = 0, 1
 MLA_ACT_BF16, MLA_ACT_FP32 = 0, 1
 MLA_ROPE_NEOX, MLA_ROPE_INTERLEAVED = 0, 1
+MLA_W_BF16, MLA_W_FP8_E4M3 = 0, 1
 D_QK, D_V = 576, 512
 
 DEVICE_ERRORS = {0: "ok", 1: "kv index out of range", 2: "decreasing indptr",
@@ -80,6 +81,15 @@ class RopeArgs(ctypes.Structure):
                 ("kv_scale", ctypes.c_float)]
 
 
+class BmmArgs(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("x_stride_token", ctypes.c_int64), ("x_stride_head", ctypes.c_int64),
+                ("w", ctypes.c_void_p), ("w_dtype", ctypes.c_int32), ("w_scale", ctypes.c_float),
+                ("out", ctypes.c_void_p), ("out_stride_token", ctypes.c_int64),
+                ("out_stride_head", ctypes.c_int64), ("num_tokens", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("k", ctypes.c_int32), ("n", ctypes.c_int32),
+                ("status_d", ctypes.c_void_p)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run `python -c 'import __graft_entry__ as g; "
@@ -98,6 +108,7 @@ def _load():
         "mla_merge_states": (ctypes.c_int, [vp, i32, vp, i32, i64, i32, vp, i32, vp, vp]),
         "mla_cache_write": (ctypes.c_int, [ctypes.POINTER(CacheWriteArgs), vp]),
         "mla_rope_q_cache": (ctypes.c_int, [ctypes.POINTER(RopeArgs), vp]),
+        "mla_absorb_bmm": (ctypes.c_int, [ctypes.POINTER(BmmArgs), vp]),
         "mla_get_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
@@ -112,7 +123,8 @@ _lib = _load()
 # Symbols the header declares; tests check the library exports each one.
 ABI_SYMBOLS = ("mla_abi_version", "mla_status_string", "mla_decode_plan_size", "mla_decode_plan",
                "mla_decode_plan_device", "mla_decode_fwd", "mla_merge_states",
-               "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write", "mla_rope_q_cache")
+               "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write", "mla_rope_q_cache",
+               "mla_absorb_bmm")
 
 
 def library():
@@ -294,3 +306,33 @@ def mla_get_device_error(workspace_d, stream=None) -> Tuple[int, int]:
 
 
 from .runner import DecodeRunner  # noqa: E402  (plumbing: buffers + calls, no compute)
+
+
+def mla_absorb_bmm(x, w, out, w_scale: float = 1.0, status=None, stream=None) -> None:
+    """Per-head product out[t, h] = bf16(w_scale * x[t, h] @ w[h]).
+
+    x bf16 [n, H, k] and out bf16 [n, H, n_out] (unit stride along the last dim,
+    any token/head strides, e.g. a column slice of the 576-wide q); w [H, k, n_out]
+    contiguous, bf16 or uint8 holding e4m3fn codes (float8_e4m3fn also accepted);
+    status: optional int32 [2] device tensor for a wait timeout record."""
+    import torch
+    if x.dtype != torch.bfloat16 or out.dtype != torch.bfloat16 or x.stride(-1) != 1 or out.stride(-1) != 1:
+        raise MlaError(1, "mla_absorb_bmm: x and out must be bf16 with unit stride along the last dim")
+    if not w.is_contiguous():
+        raise MlaError(1, "mla_absorb_bmm: w must be contiguous [H, k, n]")
+    if w.dtype == torch.bfloat16:
+        w_dtype = MLA_W_BF16
+    elif w.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        w_dtype = MLA_W_FP8_E4M3
+    else:
+        raise MlaError(1, f"mla_absorb_bmm: unsupported weight dtype {w.dtype}")
+    if w.dim() != 3 or x.dim() != 3 or out.dim() != 3 or w.shape[0] != x.shape[1] or w.shape[1] != x.shape[2] \
+            or out.shape[:2] != x.shape[:2] or out.shape[2] != w.shape[2]:
+        raise MlaError(1, "mla_absorb_bmm: shapes must be x [n, H, k], w [H, k, m], out [n, H, m]")
+    a = BmmArgs()
+    a.x, a.x_stride_token, a.x_stride_head = _ptr(x), x.stride(0), x.stride(1)
+    a.w, a.w_dtype, a.w_scale = _ptr(w), w_dtype, w_scale
+    a.out, a.out_stride_token, a.out_stride_head = _ptr(out), out.stride(0), out.stride(1)
+    a.num_tokens, a.num_heads, a.k, a.n = int(x.shape[0]), int(x.shape[1]), int(x.shape[2]), int(w.shape[2])
+    a.status_d = _ptr(status)
+    _check(_lib.mla_absorb_bmm(ctypes.byref(a), _stream(stream)), "mla_absorb_bmm")

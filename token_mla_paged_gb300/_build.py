@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmla_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["abi.cpp", "plan_host.cpp", "plan_device.cu", "merge.cu", "decode_cuda_core.cu",
-           "decode_tensor.cu", "noalloc.cu", "cache_write.cu"]
+           "decode_tensor.cu", "noalloc.cu", "cache_write.cu", "absorb_bmm.cu"]
 
 
 def _nvcc() -> str:

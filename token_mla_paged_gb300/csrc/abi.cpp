@@ -214,6 +214,25 @@ mla_status mla_rope_q_cache(const mla_rope_q_cache_args* a, void* stream) {
   return launch_rope_q_cache(*a, stream);
 }
 
+mla_status mla_absorb_bmm(const mla_absorb_bmm_args* a, void* stream) {
+  if (!a) return MLA_ERR_INVALID_ARG;
+  if (a->num_tokens < 0 || a->num_heads < 1 || a->num_heads > 65535) return MLA_ERR_INVALID_ARG;
+  if (a->k < 64 || a->k > 8192 || a->k % 64 != 0 || a->n < 128 || a->n > 8192 || a->n % 128 != 0)
+    return MLA_ERR_INVALID_ARG;
+  if (a->w_dtype != MLA_W_BF16 && a->w_dtype != MLA_W_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(a->w_scale)) return MLA_ERR_INVALID_ARG;
+  if (a->x_stride_head < a->k || a->out_stride_head < a->n || a->x_stride_token < 0 || a->out_stride_token < 0)
+    return MLA_ERR_INVALID_ARG;
+  const int64_t strides[] = {a->x_stride_token, a->x_stride_head, a->out_stride_token, a->out_stride_head};
+  for (int64_t st : strides)
+    if (st % 8 != 0) return MLA_ERR_INVALID_ARG;
+  if (a->num_tokens == 0) return MLA_OK;
+  if (!a->x || !a->w || !a->out) return MLA_ERR_INVALID_ARG;
+  if (!aligned(a->x, 16) || !aligned(a->w, 16) || !aligned(a->out, 16) || !aligned(a->status_d, 4))
+    return MLA_ERR_INVALID_ARG;
+  return launch_absorb_bmm(*a, stream);
+}
+
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info) {
   if (!workspace_d || !code) return MLA_ERR_INVALID_ARG;
   int32_t h[2] = {0, 0};

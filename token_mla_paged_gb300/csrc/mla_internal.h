@@ -118,6 +118,7 @@ mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const floa
                                void* stream);
 mla_status launch_cache_write(const mla_cache_write_args& a, void* stream);
 mla_status launch_rope_q_cache(const mla_rope_q_cache_args& a, void* stream);
+mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream);
 int tensor_kernel_available();
 
 }  // namespace mla
