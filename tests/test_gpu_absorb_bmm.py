@@ -8,7 +8,8 @@ must satisfy |y - y*| <= 2^-8 |y*| + 2^-14 * |s| * sum_k |x_k w_k|.
 
 Covered: the absorb shape (k=128, n=512) and the un-absorb shape (k=512, n=128),
 bf16 and fp8 weights, token counts from 1 to 300 (one to two token tiles, ragged
-tails), strided activations (q_nope as a view of a [n, H, 192] projection) and a
+tails), every fp8 code and bf16 subnormal weights bit-exact through a
+one-hot x, strided activations (q_nope as a view of a [n, H, 192] projection) and a
 strided output (the first 512 columns of the 576-wide decode q, the RoPE columns
 left untouched), zero tokens, repeatability, CUDA-graph replay, the full-size
 workload (256 tokens x 128 heads), and the absorb -> decode -> un-absorb chain
@@ -174,6 +175,46 @@ def test_absorb_decode_unabsorb_chain():
     got = _to_f64(out)
     rms = np.sqrt(np.mean(ref ** 2))
     assert np.all(np.abs(got - ref) <= 2e-2 * (np.abs(ref) + rms))
+
+
+def _one_hot_x(tokens, heads, k):
+    x = np.zeros((tokens, heads, k), np.float32)
+    x[np.arange(tokens), :, np.arange(tokens) % k] = 1.0
+    return mi.to_bf16_bits(x)
+
+
+def test_every_fp8_code_is_exact():
+    """A one-hot x picks one weight row per token, so each output is the single
+    product bf16(fp32(w) * fp32(s)): every finite e4m3fn code (subnormals, zeros of
+    both signs, +-448) must come out bit-exact."""
+    H, K, N = 2, 128, 512
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    w_bits = np.resize(codes, H * K * N).reshape(H, K, N)
+    w_bits[1] = np.roll(w_bits[1], 37, axis=1)
+    scale = 0.3711
+    inp = mi.BmmInputs(x_bits=_one_hot_x(K, H, K), w_bits=w_bits, w_dtype="fp8", w_scale=scale)
+    y = _run(inp).view(torch.int16).cpu().numpy().view(np.uint16)
+    wv = fm.decode_e4m3fn(w_bits).astype(np.float32)                     # exact
+    t = np.arange(K)
+    want = cw.f32_to_bf16_rne((wv[:, t % K, :] * np.float32(scale)).astype(np.float32)).transpose(1, 0, 2)
+    # a -0 product summed with the +0 products of the other rows is +0 (IEEE)
+    same = (y == want) | (((y & 0x7FFF) == 0) & ((want & 0x7FFF) == 0))
+    bad = np.argwhere(~same)
+    assert bad.size == 0, [(int(w_bits[h, tt % K, j]), int(y[tt, h, j]), int(want[tt, h, j])) for tt, h, j in bad[:8]]
+
+
+def test_bf16_weights_including_subnormals_are_exact():
+    rng = np.random.default_rng(17)
+    H, K, N = 3, 64, 256
+    w = rng.standard_normal((H, K, N)).astype(np.float32) * rng.choice(
+        np.array([1e-39, 1e-30, 1e-3, 1.0, 300.0], np.float32), size=(H, K, N))
+    inp = mi.BmmInputs(x_bits=_one_hot_x(K, H, K), w_bits=mi.to_bf16_bits(w), w_dtype="bf16", w_scale=1.0)
+    y = _run(inp).view(torch.int16).cpu().numpy().view(np.uint16)
+    t = np.arange(K)
+    want = inp.w_bits[:, t % K, :].transpose(1, 0, 2)
+    same = (y == want) | (((y & 0x7FFF) == 0) & ((want & 0x7FFF) == 0))
+    bad = np.argwhere(~same)
+    assert bad.size == 0, [(int(y[tt, h, j]), int(want[tt, h, j])) for tt, h, j in bad[:8]]
 
 
 def test_rejects_bad_arguments():

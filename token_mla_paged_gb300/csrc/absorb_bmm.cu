@@ -4,27 +4,27 @@
 //   after:  out[t, h, :]   = o_lat[t, h, :]  @ W_UV[h]     (k = 512, n = 128)
 // One kernel computes y[t, h, j] = bf16(s * sum_k x[t, h, k] * w[h, k, j]).
 //
-// A decode step has few tokens and many heads, so the product is computed
-// transposed, D[j, t] = sum_k w[h, k, j] * x[t, h, k], with the weight as the
-// M = 128 operand and the tokens as the N operand (16..256 wide): one CTA per
-// (head, 128 weight columns, token tile), no padding of a small token count to
-// 128 rows.  Per 64-wide k chunk, TMA brings
-//   * the weight tile, [64 k][128 j]: bf16 as two 128-byte-swizzled boxes of 64 j
-//     (the MN-major A operand of tcgen05.mma), fp8 as one raw 128-byte box that four
-//     conversion warps expand exactly to bf16 in that same layout;
-//   * the token tile, [tok_tile t][64 k] bf16, 128-byte swizzled (the K-major B
-//     operand); rows past the last token are zero-filled by the TMA.
-// Four MMAs (K = 16 each) per chunk accumulate D[128, tok_tile] fp32 in TMEM.  The
-// epilogue warps read their 32 TMEM lanes (32 output columns j), scale, round to
-// bf16 and transpose through 2 KB of shared memory per warp so each token's 32
-// columns leave as one 64-byte segment.
-//
-// Warp roles (192 threads): 0 TMA producer, 1 TMEM allocation + MMA issue, 2-5
-// fp8 conversion during the main loop and the epilogue after it.  Every barrier
-// wait is bounded; a wait that runs out records MLA_DEV_WAIT_TIMEOUT (and the
-// wait site) in the optional status word, raises an abort flag, and the CTA
-// drains its copies and MMAs in flight (again bounded) before it frees TMEM and
-// returns.
+// The work is HBM-bound (each weight byte and each activation byte is used a few
+// hundred times at most), so the kernel is built to keep every SM streaming:
+//   * a unit is (head, 128 tokens, 128 output columns); one persistent CTA per
+//     SM walks its units in a fixed stride;
+//   * per 64-wide k chunk TMA brings the token tile [128 t][64 k] (bf16, 128-byte
+//     swizzled: the K-major A operand, rows past the last token zero-filled) and
+//     the weight tile [64 k][128 j] (bf16 as 64-column swizzled boxes: the
+//     MN-major B operand; fp8 as one raw box that eight conversion warps expand
+//     exactly to bf16 in that same layout), through a ring of stages that runs
+//     across unit boundaries;
+//   * four tcgen05.mma (M=128, N=128, K=16) per chunk accumulate D[t, j] in one
+//     of two TMEM accumulators, so the epilogue of a unit overlaps the loads and
+//     MMAs of the next;
+//   * each epilogue warp owns 32 token rows x 64 columns: TMEM -> registers, times s,
+//     rounded to bf16, staged in 2 KB of XOR-swizzled shared memory per warp and
+//     written as whole 64-byte row segments.
+// Warp roles: 0 TMA producer, 1 TMEM allocation + MMA issue, 2-9 epilogue (two
+// per TMEM lane quadrant, 64 columns each), 10-17 fp8 conversion (fp8 only).  Every barrier wait is bounded; a wait
+// that runs out records MLA_DEV_WAIT_TIMEOUT (and the wait site) in the optional
+// status word and raises an abort flag; the CTA then lets its copies and MMAs in
+// flight complete (bounded waits again), frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,24 +37,27 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;
-constexpr int kKChunk = 64;                    // k per pipeline stage
-constexpr int kWTileBytes = 128 * kKChunk * 2;  // bf16 weight tile [64 k][128 j]
-constexpr int kWBlockBytes = kWTileBytes / 2;   // one 64-column block of it
-constexpr int kWRawBytes = 128 * kKChunk;       // fp8 weight tile
-constexpr int kMaxStages = 4;
+constexpr int kKChunk = 64;                   // k per pipeline stage
+constexpr int kTokTile = 128;                 // M of the MMA
+constexpr int kNTile = 128;                   // N of the MMA: output columns per unit
+constexpr int kXBytes = kTokTile * 128;       // token tile per chunk (16 KB)
+constexpr int kWBlockBytes = 64 * 128;        // bf16 weight block [64 k][64 j]
+constexpr int kMaxStages = 6;
 constexpr int kSmemAlign = 1024;
+constexpr int kEpiWarps = 8;                  // two per TMEM lane quadrant, 64 columns each
+constexpr int kEpiBytes = kEpiWarps * 2048;   // per-warp staging of the epilogue
+
+constexpr int kConvWarps = 8;                 // fp8 weight conversion
+__host__ __device__ constexpr int threads_for(bool fp8) { return 32 * (2 + kEpiWarps + (fp8 ? kConvWarps : 0)); }
 
 struct BmmParams {
   __nv_bfloat16* out;
   long long o_ts, o_hs;  // elements
   float w_scale;
   int n_tok, H, K, N;
-  int tok_tile;          // multiple of 16, 16..256
-  int stages;            // 1..kMaxStages
-  int n_mtiles;          // N / 128
-  int tmem_cols;         // power of two >= max(32, tok_tile)
-  int stage_bytes;       // bf16 weight tile + token tile (+ raw fp8 tile)
+  int stages;            // 2..kMaxStages
+  int n_ttiles, n_jtiles, units;
+  int stage_bytes;       // token tile + bf16 weight tile (+ raw fp8 tile)
   int32_t* status;       // optional
 };
 
@@ -62,7 +65,8 @@ struct BmmBars {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t conv[kMaxStages];
-  uint64_t acc_full;
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
   uint64_t drain;
   uint32_t tmem_slot;
   int abort;
@@ -77,15 +81,21 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
-// Two e4m3fn codes (low byte first) -> two bf16 values, exactly: e4m3 -> f16 is
-// exact, f16 -> f32 is exact, and every e4m3 value is a bf16 value.
+// Two e4m3fn codes (low byte first) -> two bf16 values, exactly.  e4m3 -> f16
+// is exact (one conversion instruction for the pair); every such f16 has at
+// most 3 significant mantissa bits and is normal (e4m3's subnormals are f16
+// normals), so the bf16 keeps the sign, drops the 3 low mantissa bits and
+// re-biases the exponent from 15 to 127 (+112); zeros stay zero.  The NaN codes
+// 0x7F / 0xFF are outside the contract (they come out finite).
 __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-  float lo, hi;
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-      : "=f"(lo), "=f"(hi)
-      : "r"(h2));
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  const uint32_t mag = h & 0x7FFF7FFFu;
+  const uint32_t bias = ((mag & 0xFFFFu) ? 0x3800u : 0u) | ((mag >> 16) ? 0x38000000u : 0u);
+  return (((mag >> 3) & 0x0FFF0FFFu) + bias) | (h & 0x80008000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
@@ -96,30 +106,74 @@ __device__ __forceinline__ void record_timeout(const BmmParams& p, volatile int*
   *abort = 1;
 }
 
+struct Unit {
+  int h, t0, j0;
+};
+__device__ __forceinline__ Unit unit_of(const BmmParams& p, int u) {
+  Unit r;
+  r.h = u / (p.n_ttiles * p.n_jtiles);
+  const int rem = u - r.h * (p.n_ttiles * p.n_jtiles);
+  r.t0 = (rem / p.n_jtiles) * kTokTile;
+  r.j0 = (rem % p.n_jtiles) * kNTile;
+  return r;
+}
+
+// Bounded wait in which the thread sleeps in the barrier until the phase
+// completes (or 0.5 ms pass) instead of spinning, so waiting warps leave the
+// shared-memory pipe to the warps that work.  Gives up after about a second, or
+// when *abort is set.
+__device__ __forceinline__ bool try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(500000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (try_wait_suspend(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (try_wait_suspend(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  }
+}
+
+#define BMM_WAIT(bar, parity, site, label)                   \
+  if (!wait_phase((bar), (parity), abort)) {                 \
+    if (!*abort) record_timeout(p, abort, (site));           \
+    goto label;                                              \
+  }
+
 template <bool kFp8>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kFp8), 1)
     mla_absorb_bmm_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_w,
                           const BmmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + kSmemAlign - 1) & ~(uintptr_t)(kSmemAlign - 1));
-  BmmBars* bars = reinterpret_cast<BmmBars*>(smem + p.stages * p.stage_bytes);
+  uint8_t* epi = smem + p.stages * p.stage_bytes;
+  BmmBars* bars = reinterpret_cast<BmmBars*>(epi + kEpiBytes);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mtile = blockIdx.x % p.n_mtiles, ttile = blockIdx.x / p.n_mtiles;
-  const int h = blockIdx.y;
-  const int m0 = mtile * 128, t0 = ttile * p.tok_tile;
   const int nk = p.K / kKChunk;
-  const int x_bytes = p.tok_tile * 128;
+  const int wbytes = kNTile * 128;             // bf16 weight tile per chunk
+  const int nblk = kNTile / 64;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&bars->full[s], 1);
       mbar_init(&bars->empty[s], 1);
-      mbar_init(&bars->conv[s], 128);
+      mbar_init(&bars->conv[s], 32 * kConvWarps);
     }
-    mbar_init(&bars->acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars->acc_full[b], 1);
+      mbar_init(&bars->acc_empty[b], 32 * kEpiWarps);
+    }
     mbar_init(&bars->drain, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -127,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmap_w);
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_slot, (uint32_t)p.tmem_cols);
+    tmem_alloc(&bars->tmem_slot, (uint32_t)(2 * kNTile));
     tmem_relinquish();
   }
   fence_before_sync();
@@ -139,30 +193,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int issued = 0;
-      for (int c = 0; c < nk; ++c) {
-        const int s = c % p.stages;
-        if (!mbar_wait(&bars->empty[s], ((c / p.stages) & 1) ^ 1, abort)) {
-          if (!*abort) record_timeout(p, abort, 1);
-          break;
+      uint32_t g = 0, issued_from = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Unit un = unit_of(p, u);
+        for (int c = 0; c < nk; ++c, ++g) {
+          const int s = (int)(g % p.stages);
+          BMM_WAIT(&bars->empty[s], ((g / p.stages) & 1) ^ 1, 1, done_producer);
+          const uint32_t st = sbase + (uint32_t)(s * p.stage_bytes);
+          mbar_arrive_expect_tx(&bars->full[s], (uint32_t)(kXBytes + (kFp8 ? kNTile * kKChunk : wbytes)));
+          tma_load_3d(st, &tmap_x, c * kKChunk, un.h, un.t0, &bars->full[s]);
+          if (kFp8) {
+            tma_load_3d(st + kXBytes + wbytes, &tmap_w, un.j0, c * kKChunk, un.h, &bars->full[s]);
+          } else {
+            for (int b = 0; b < nblk; ++b)
+              tma_load_3d(st + kXBytes + b * kWBlockBytes, &tmap_w, un.j0 + 64 * b, c * kKChunk, un.h,
+                          &bars->full[s]);
+          }
         }
-        const uint32_t st = sbase + (uint32_t)(s * p.stage_bytes);
-        mbar_arrive_expect_tx(&bars->full[s], (uint32_t)(x_bytes + (kFp8 ? kWRawBytes : kWTileBytes)));
-        tma_load_3d(st + kWTileBytes, &tmap_x, c * kKChunk, h, t0, &bars->full[s]);
-        if (kFp8) {
-          tma_load_3d(st + kWTileBytes + x_bytes, &tmap_w, m0, c * kKChunk, h, &bars->full[s]);
-        } else {
-          tma_load_3d(st, &tmap_w, m0, c * kKChunk, h, &bars->full[s]);
-          tma_load_3d(st + kWBlockBytes, &tmap_w, m0 + 64, c * kKChunk, h, &bars->full[s]);
-        }
-        ++issued;
       }
+    done_producer:
       if (*abort) {
         // Let the copies already issued land before the shared memory goes away.
-        for (int c = issued > p.stages ? issued - p.stages : 0; c < issued; ++c) {
-          const int s = c % p.stages;
+        issued_from = g > (uint32_t)p.stages ? g - p.stages : 0;
+        for (uint32_t c = issued_from; c < g; ++c) {
           const long long t0c = clock64();
-          while (!mbar_try_wait(&bars->full[s], (c / p.stages) & 1) && clock64() - t0c < kWaitLimitCycles) {
+          while (!mbar_try_wait(&bars->full[c % p.stages], (c / p.stages) & 1) &&
+                 clock64() - t0c < kWaitLimitCycles) {
           }
         }
       }
@@ -170,108 +226,132 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issue
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, p.tok_tile, true, false);
-      int issued = 0;
-      for (int c = 0; c < nk; ++c) {
-        const int s = c % p.stages;
-        const uint32_t ph = (c / p.stages) & 1;
-        if (!mbar_wait(kFp8 ? &bars->conv[s] : &bars->full[s], ph, abort)) {
-          if (!*abort) record_timeout(p, abort, 2);
-          break;
-        }
+      const uint32_t idesc = idesc_bf16_f32(kTokTile, kNTile, false, true);
+      uint32_t g = 0, i = 0;
+      bool any = false;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+        const uint32_t buf = i & 1;
+        BMM_WAIT(&bars->acc_empty[buf], ((i >> 1) & 1) ^ 1, 2, done_mma);
         fence_after_sync();
-        const uint32_t st = sbase + (uint32_t)(s * p.stage_bytes);
-        const uint64_t adesc = smem_desc_sw128(st, kWBlockBytes, 1024);
-        const uint64_t bdesc = smem_desc_sw128(st + kWTileBytes, 16, 1024);
+        for (int c = 0; c < nk; ++c, ++g) {
+          const int s = (int)(g % p.stages);
+          BMM_WAIT(kFp8 ? &bars->conv[s] : &bars->full[s], (g / p.stages) & 1, 3, done_mma);
+          fence_after_sync();
+          const uint32_t st = sbase + (uint32_t)(s * p.stage_bytes);
+          const uint64_t adesc = smem_desc_sw128(st, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(st + kXBytes, kWBlockBytes, 1024);
 #pragma unroll
-        for (int k = 0; k < kKChunk / 16; ++k)
-          mma_ss(tmem, adesc + (uint64_t)((k * 2048) >> 4), bdesc + (uint64_t)((k * 32) >> 4), idesc,
-                 (c > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bars->empty[s]);
-        ++issued;
-      }
-      if (*abort) {
-        if (issued > 0) {
-          mma_commit(&bars->drain);
-          const long long t0c = clock64();
-          while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0c < kWaitLimitCycles) {
-          }
+          for (int k = 0; k < kKChunk / 16; ++k)
+            mma_ss(tmem + buf * (uint32_t)kNTile, adesc + (uint64_t)((k * 32) >> 4),
+                   bdesc + (uint64_t)((k * 2048) >> 4), idesc, (c > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bars->empty[s]);
+          any = true;
         }
-      } else {
-        mma_commit(&bars->acc_full);
+        mma_commit(&bars->acc_full[buf]);
+      }
+    done_mma:
+      if (*abort && any) {
+        mma_commit(&bars->drain);
+        const long long t0c = clock64();
+        while (!mbar_try_wait(&bars->drain, 0) && clock64() - t0c < kWaitLimitCycles) {
+        }
       }
     }
     __syncwarp();
-  } else {
-    // ------------------------------------------------------------ warps 2-5
-    const int tid = threadIdx.x - 64;  // 0..127
-    bool ok = true;
-    if (kFp8) {
-      for (int c = 0; c < nk && ok; ++c) {
-        const int s = c % p.stages;
-        if (!mbar_wait(&bars->full[s], (c / p.stages) & 1, abort)) {
-          if (!*abort) record_timeout(p, abort, 3);
-          ok = false;
-          break;
-        }
-        uint8_t* st = smem + s * p.stage_bytes;
-        const uint8_t* raw = st + kWTileBytes + x_bytes;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = tid + 128 * i;          // 16-byte unit of the raw tile: 64 rows x 8
-          const int kr = u >> 3, col = (u & 7) * 16;
-          const uint4 v = *reinterpret_cast<const uint4*>(raw + kr * 128 + col);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            o[2 * q] = e4m3x2_to_bf16x2((uint16_t)(w4[q] & 0xFFFFu));
-            o[2 * q + 1] = e4m3x2_to_bf16x2((uint16_t)(w4[q] >> 16));
-          }
-          const int blk = col >> 6, uu = (col & 63) >> 3;  // 64-column block, 16-byte unit in its line
-          uint8_t* line = st + blk * kWBlockBytes + kr * 128;
-          *reinterpret_cast<uint4*>(line + ((uu ^ (kr & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(line + (((uu + 1) ^ (kr & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars->conv[s]);
-      }
-    }
-    if (ok && mbar_wait(&bars->acc_full, 0, abort)) {
+  } else if (warp < 2 + kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;                   // TMEM lanes = token rows 32*quad .. +31
+    const int half = (warp - 2) >> 2;            // columns 64*half .. +63
+    uint8_t* stg = epi + (warp - 2) * 2048;
+    uint32_t i = 0;
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+      const Unit un = unit_of(p, u);
+      const uint32_t buf = i & 1;
+      BMM_WAIT(&bars->acc_full[buf], (i >> 1) & 1, 4, done_epilogue);
       fence_after_sync();
-      const int quad = warp & 3;                      // TMEM lanes 32*quad .. +31
-      uint8_t* stg = smem + (warp - 2) * 2048;        // stage memory is free once D is complete
-      __nv_bfloat16* stg_h = reinterpret_cast<__nv_bfloat16*>(stg);
-      const int jcol = m0 + 32 * quad;
-      for (int j0 = 0; j0 < p.tok_tile; j0 += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)j0, r);
+      uint32_t acc[2][32];
+      {
+        const uint32_t ta = tmem + buf * (uint32_t)kNTile + ((uint32_t)(32 * quad) << 16) + 64 * half;
+        tmem_ld32(ta, acc[0]);
+        tmem_ld32(ta + 32, acc[1]);
         tmem_wait_ld();
+      }
+      fence_before_sync();
+      mbar_arrive(&bars->acc_empty[buf]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          stg_h[i * 32 + lane] = __float2bfloat16_rn(__uint_as_float(r[i]) * p.w_scale);
+      for (int g2 = 0; g2 < 2; ++g2) {
+        const int c0 = 64 * half + 32 * g2;
+        const uint32_t* r = acc[g2];
+        // row `lane` of the staging block: 4 units of 8 columns, XOR-swizzled by row
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * p.w_scale, __uint_as_float(r[8 * q + 1]) * p.w_scale);
+          v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * p.w_scale, __uint_as_float(r[8 * q + 3]) * p.w_scale);
+          v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * p.w_scale, __uint_as_float(r[8 * q + 5]) * p.w_scale);
+          v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * p.w_scale, __uint_as_float(r[8 * q + 7]) * p.w_scale);
+          *reinterpret_cast<uint4*>(stg + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = v;
+        }
         __syncwarp();
 #pragma unroll
         for (int pass = 0; pass < 4; ++pass) {
-          const int ti = pass * 8 + (lane >> 2);
-          const int t = t0 + j0 + ti;
-          if (j0 + ti < p.tok_tile && t < p.n_tok) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stg + ti * 64 + (lane & 3) * 16);
-            *reinterpret_cast<uint4*>(p.out + (long long)t * p.o_ts + (long long)h * p.o_hs + jcol +
-                                      (lane & 3) * 8) = v;
-          }
+          const int row = pass * 8 + (lane >> 2), q = lane & 3;
+          const int t = un.t0 + 32 * quad + row;
+          const uint4 v = *reinterpret_cast<const uint4*>(stg + row * 64 + ((q ^ ((row >> 1) & 3)) << 4));
+          if (t < p.n_tok)
+            *reinterpret_cast<uint4*>(p.out + (long long)t * p.o_ts + (long long)un.h * p.o_hs + un.j0 + c0 +
+                                      8 * q) = v;
         }
         __syncwarp();
       }
-    } else if (ok && !*abort) {
-      record_timeout(p, abort, 4);
+    }
+  done_epilogue:;
+  } else {
+    // ------------------------------------------------------------ fp8 conversion
+    if (kFp8) {
+      const int tid = threadIdx.x - 32 * (2 + kEpiWarps);   // 0 .. 32 * kConvWarps - 1
+      constexpr int upr = kNTile / 8;            // 8-byte raw groups per k row
+      constexpr int iters = kKChunk * upr / (32 * kConvWarps);
+      uint32_t g = 0;
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        for (int c = 0; c < nk; ++c, ++g) {
+          const int s = (int)(g % p.stages);
+          BMM_WAIT(&bars->full[s], (g / p.stages) & 1, 5, done_convert);
+          uint8_t* st = smem + s * p.stage_bytes + kXBytes;
+          const uint8_t* raw = st + wbytes;
+          // thread -> 8 consecutive columns of one k row: eight neighbouring threads
+          // fill one 128-byte line of the swizzled tile, so the stores do not
+          // conflict; all raw words are loaded first so the conversions overlap
+          uint2 x[iters];
+#pragma unroll
+          for (int it = 0; it < iters; ++it) {
+            const int v = tid + 32 * kConvWarps * it, kr = v / upr, col = (v - kr * upr) * 8;
+            x[it] = *reinterpret_cast<const uint2*>(raw + kr * kNTile + col);
+          }
+#pragma unroll
+          for (int it = 0; it < iters; ++it) {
+            const int v = tid + 32 * kConvWarps * it, kr = v / upr, col = (v - kr * upr) * 8;
+            const uint4 o = make_uint4(e4m3x2_to_bf16x2((uint16_t)(x[it].x & 0xFFFFu)),
+                                       e4m3x2_to_bf16x2((uint16_t)(x[it].x >> 16)),
+                                       e4m3x2_to_bf16x2((uint16_t)(x[it].y & 0xFFFFu)),
+                                       e4m3x2_to_bf16x2((uint16_t)(x[it].y >> 16)));
+            const int blk = col >> 6, uu = (col & 63) >> 3;   // 64-column block, unit in its line
+            *reinterpret_cast<uint4*>(st + blk * kWBlockBytes + kr * 128 + ((uu ^ (kr & 7)) << 4)) = o;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->conv[s]);
+        }
+      }
+    done_convert:;
     }
   }
 
   fence_before_sync();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  if (warp == 1) tmem_dealloc(tmem, (uint32_t)(2 * kNTile));
 }
+
+#undef BMM_WAIT
 
 // ----------------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -292,10 +372,12 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-int pow2_at_least(int v) {
-  int r = 1;
-  while (r < v) r <<= 1;
-  return r;
+int sm_count() {
+  static int n[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 0;
+  return n[dev];
 }
 
 }  // namespace
@@ -303,7 +385,8 @@ int pow2_at_least(int v) {
 mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
   if (a.num_tokens == 0) return MLA_OK;
   EncodeTiledFn enc = encoder();
-  if (!enc) return MLA_ERR_CUDA;
+  const int sms = sm_count();
+  if (!enc || sms <= 0) return MLA_ERR_CUDA;
   const bool fp8 = a.w_dtype == MLA_W_FP8_E4M3;
 
   BmmParams p;
@@ -315,29 +398,30 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
   p.H = a.num_heads;
   p.K = a.k;
   p.N = a.n;
-  p.tok_tile = a.num_tokens >= 256 ? 256 : (a.num_tokens + 15) / 16 * 16;
-  p.n_mtiles = a.n / 128;
-  p.tmem_cols = pow2_at_least(p.tok_tile < 32 ? 32 : p.tok_tile);
-  p.stage_bytes = kWTileBytes + p.tok_tile * 128 + (fp8 ? kWRawBytes : 0);
+  p.n_ttiles = (a.num_tokens + kTokTile - 1) / kTokTile;
+  p.n_jtiles = a.n / kNTile;
+  const long long units = (long long)a.num_heads * p.n_ttiles * p.n_jtiles;
+  if (units > 0x7FFFFFFFLL) return MLA_ERR_UNSUPPORTED;
+  p.units = (int)units;
+  p.stage_bytes = kXBytes + kNTile * 128 + (fp8 ? kNTile * kKChunk : 0);
   p.status = a.status_d;
-  const int nk = a.k / kKChunk;
   const int bar_bytes = (int)((sizeof(BmmBars) + 127) / 128 * 128);
-  const int smem_cap = 227 * 1024 - kSmemAlign - bar_bytes;
-  p.stages = nk < kMaxStages ? nk : kMaxStages;
-  while (p.stages > 1 && p.stages * p.stage_bytes > smem_cap) --p.stages;
+  const int smem_cap = 227 * 1024 - kSmemAlign - kEpiBytes - bar_bytes;
+  p.stages = kMaxStages;
+  while (p.stages > 2 && p.stages * p.stage_bytes > smem_cap) --p.stages;
   if (p.stages * p.stage_bytes > smem_cap) return MLA_ERR_UNSUPPORTED;
-  int smem = p.stages * p.stage_bytes + bar_bytes + kSmemAlign;
-  // Never more CTAs on an SM than its 512 TMEM columns hold, so an allocation
-  // never waits for another CTA: request enough shared memory to cap residency.
-  const int max_ctas = 512 / p.tmem_cols;
-  const int min_smem = 228 * 1024 / (max_ctas + 1) + 1024;
-  if (smem < min_smem) smem = min_smem;
+  int smem = p.stages * p.stage_bytes + kEpiBytes + bar_bytes + kSmemAlign;
+  // One CTA per SM (its ring fills the shared memory); the request never drops
+  // below half the SM's shared memory, so two CTAs' accumulators (2 x 256 TMEM
+  // columns) are the most an SM could ever be asked for.
+  const int one_cta = 228 * 1024 / 2 + 1024;
+  if (smem < one_cta) smem = one_cta;
 
   CUtensorMap tx, tw;
   {
     const cuuint64_t gdim[3] = {(cuuint64_t)a.k, (cuuint64_t)a.num_heads, (cuuint64_t)a.num_tokens};
     const cuuint64_t gstride[2] = {(cuuint64_t)a.x_stride_head * 2, (cuuint64_t)a.x_stride_token * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)kKChunk, 1u, (cuuint32_t)p.tok_tile};
+    const cuuint32_t box[3] = {(cuuint32_t)kKChunk, 1u, (cuuint32_t)kTokTile};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.x), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -348,7 +432,7 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
     const int esz = fp8 ? 1 : 2;
     const cuuint64_t gdim[3] = {(cuuint64_t)a.n, (cuuint64_t)a.k, (cuuint64_t)a.num_heads};
     const cuuint64_t gstride[2] = {(cuuint64_t)a.n * esz, (cuuint64_t)a.n * a.k * esz};
-    const cuuint32_t box[3] = {fp8 ? 128u : 64u, (cuuint32_t)kKChunk, 1u};
+    const cuuint32_t box[3] = {fp8 ? (cuuint32_t)kNTile : 64u, (cuuint32_t)kKChunk, 1u};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&tw, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.w),
             gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -356,8 +440,7 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return MLA_ERR_INVALID_ARG;
   }
-  const int n_ttiles = (a.num_tokens + p.tok_tile - 1) / p.tok_tile;
-  const dim3 grid((unsigned)(p.n_mtiles * n_ttiles), (unsigned)a.num_heads, 1);
+  const int grid = p.units < sms ? p.units : sms;
   // The shared-memory limit is raised once per kernel (to the largest size any
   // call needs), outside stream capture in the usual first-call-then-capture order.
   static int smem_set[2] = {0, 0};
@@ -367,7 +450,7 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
       return MLA_ERR_CUDA;
     smem_set[fp8] = smem;
   }
-  kern<<<grid, kThreads, smem, (cudaStream_t)stream>>>(tx, tw, p);
+  kern<<<grid, threads_for(fp8), smem, (cudaStream_t)stream>>>(tx, tw, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
