@@ -334,7 +334,9 @@ typedef struct {
  *   out[t, h, j] = bf16( w_scale * sum_k x[t, h, k] * w[h, k, j] )
  * with an fp8 weight decoded exactly (e4m3fn), products exact and summed in
  * float32 on the tensor cores, the float32 sum times w_scale rounded to bf16
- * (nearest, ties to even).  out may be a column slice of a wider buffer (e.g. the
+ * (nearest, ties to even).  The e4m3 NaN codes (0x7F, 0xFF) are outside the
+ * contract (they come out finite); sums of signed zeros follow IEEE (-0 + +0 = +0).
+ * out may be a column slice of a wider buffer (e.g. the
  * first 512 columns of the 576-wide q) through its strides.  Pointers 16-byte
  * aligned and strides multiples of 8, x_stride_head >= k, out_stride_head >= n,
  * else MLA_ERR_INVALID_ARG.  Enqueued on `stream`; nothing is read back, so the
