@@ -755,8 +755,10 @@ def main():
     shards = extra["shards"]
     algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
     sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
-    # Plan workers: the tensor kernel runs one item per CTA pair; the default per
-    # workload is the value that balanced best in the sweeps recorded in the design doc.
+    # Plan workers: the tensor kernel runs one item per CTA pair.  The draft block
+    # has 64 row groups, and 64 workers (one item per cluster, no splits) measured
+    # fastest in a sweep of worker counts; the other workloads use one worker per
+    # cluster of the GPU.
     tuned = {"draft_block_bf16": 64}
     workers = args.workers or (tuned.get(args.config, sms // 2) if algo == m.MLA_ALGO_TENSOR else sms)
     maxq = int(w.q_lens().max())
