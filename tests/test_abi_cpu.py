@@ -157,6 +157,9 @@ def test_fwd_rejects_bad_arguments_before_touching_the_device():
     a.ws_bytes = 16
     assert lib.mla_decode_fwd(ctypes.byref(a), None) == 3      # workspace too small
     a.ws_bytes = 1 << 30
+    a.workspace_d = None
+    assert lib.mla_decode_fwd(ctypes.byref(a), None) != 0     # no workspace (e.g. during capture)
+    a.workspace_d = 256
     a.q = 18
     assert lib.mla_decode_fwd(ctypes.byref(a), None) == 1      # misaligned q
     assert lib.mla_merge_states(None, 0, None, 0, 1, 512, None, 0, None, None) == 1
