@@ -8,6 +8,13 @@ of the shards) over one batch of synthetic input already resident in HBM.
   python bench.py [--config draft_block_bf16] [--steps K] [--warmup W] [--gpus N]
   python bench.py --impl reference ...     # the float64 CPU oracle on the host cores
 
+The other configs time the steps either side of the decode, each on its own
+(tokens per second, HBM roofline): cache_write_fp8 / cache_write_bf16 (KV-cache
+write), rope_cache_fp8 (fused RoPE + q concat + cache write) and absorb_bmm_fp8
+(absorb and un-absorb BMMs).  Between timed steps the L2 is flushed (a 256 MB
+write, then another 256 MB read); the timed steps are queued behind a bounded GPU
+spin so host launch cost does not sit inside the CUDA events.
+
 Under torchrun (N > 1) every rank decodes its own batch of the same shape (requests
 are independent: weak scaling, no collective on the data path); rank 0 prints the
 JSON line with the sum of units over ranks divided by the slowest rank's time.
