@@ -19,11 +19,18 @@
  *     Decode] ...", section "Three pieces");
  *   - long rows are split over the KV and merged through the LSE inside the
  *     call, driven by a split plan that is deterministic in its inputs so a
- *     CUDA-graph replay agrees with its capture; the plan is either built on
- *     the host once from capacities (STATIC) or rebuilt on the device from the
- *     real lengths at every call (DYNAMIC) ("[DSV4] Tuned ASM FP8 decode with
- *     split plans; HCA on aiter's persistent V4-NM kernel", Summary parts 1
- *     and 2).
+ *     CUDA-graph replay agrees with its capture; the plan is built on the host
+ *     once from capacities (STATIC) or from the real lengths (HOST), or rebuilt
+ *     on the device from the real lengths at every call (DYNAMIC) ("[DSV4] Tuned
+ *     ASM FP8 decode with split plans; HCA on aiter's persistent V4-NM kernel",
+ *     Summary parts 1 and 2);
+ *   - an entry may carry its own global position and causal rows may have a
+ *     sliding window, for the index lists of that page's layer types.
+ *
+ * The steps either side of the decode have their own entry points, declared
+ * at the end: mla_cache_write and mla_rope_q_cache (new tokens into the cache,
+ * q assembled for the decode) and mla_absorb_bmm (the per-head products that
+ * take q into, and O out of, the latent space).
  *
  * Definition, for request b, token t in [0,T_b), head h:
  *   k_i = dec(pool[kv_indices[kv_indptr[b]+i]]) * kappa   (kappa = kv_scale for fp8, else 1)
