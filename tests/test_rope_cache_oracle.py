@@ -2,7 +2,9 @@
 
 * the rotation against the same rotation done as complex multiplication in
   float64 (an independent formulation), within float32 rounding;
-* angle zero (cos 1, sin 0) is exactly the identity; pair norms are preserved;
+* angle zero (cos 1, sin 0) is exactly the identity, a quarter turn (cos 0, sin 1)
+  maps each pair (a, b) to (-b, a) exactly, rotating back by -theta returns the
+  input; pair norms are preserved;
 * the interleaved style is exactly the neox style on de-interleaved columns;
 * the fused outputs: q's latent columns are copied bit for bit, its RoPE
   columns are the bf16 of the rotation, the cache rows are the cache-write
@@ -97,3 +99,29 @@ def test_planted_sign_error_fails(monkeypatch):
     monkeypatch.setattr(rc, "rope_f32", wrong)
     with pytest.raises(AssertionError):
         test_rotation_matches_complex_multiplication(rc.NEOX)
+
+
+@pytest.mark.parametrize("style", [rc.NEOX, rc.INTERLEAVED])
+def test_quarter_turn_is_exact(style):
+    """cos 0, sin 1: every pair (a, b) becomes (-b, a) exactly (products by 0 and 1
+    and sums with zero are exact), which fixes the sign convention of the rotation."""
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((30, 64)).astype(np.float32)
+    zero, one = np.zeros((30, 32), np.float32), np.ones((30, 32), np.float32)
+    y = rc.rope_f32(x, zero, one, style)
+    if style == rc.NEOX:
+        a, b, ya, yb = x[:, :32], x[:, 32:], y[:, :32], y[:, 32:]
+    else:
+        a, b, ya, yb = x[:, 0::2], x[:, 1::2], y[:, 0::2], y[:, 1::2]
+    assert np.array_equal(ya, -b) and np.array_equal(yb, a)
+
+
+@pytest.mark.parametrize("style", [rc.NEOX, rc.INTERLEAVED])
+def test_rotation_then_inverse_returns_the_input(style):
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((40, 64)).astype(np.float32)
+    cs = _tables(2048)
+    p = rng.integers(0, 2048, size=40)
+    c, s = cs[p, :32], cs[p, 32:]
+    back = rc.rope_f32(rc.rope_f32(x, c, s, style), c, -s, style)
+    assert np.all(np.abs(back - x) <= 8 * np.finfo(np.float32).eps * np.abs(x).max(axis=1, keepdims=True))
