@@ -5,7 +5,7 @@ One step = one full decode call (plan as the workload needs it, attention over
 every request, split merge, and for the context-parallel workload the LSE merge
 of the shards) over one batch of synthetic input already resident in HBM.
 
-  python bench.py [--config draft_block_bf16] [--steps K] [--warmup W] [--gpus N]
+  python bench.py [--config cp_shards_bf16] [--steps K] [--warmup W] [--gpus N]
   python bench.py --impl reference ...     # the float64 CPU oracle on the host cores
 
 The other configs time the steps either side of the decode, each on its own
@@ -695,15 +695,267 @@ def absorb_main(args, rank: int, world: int):
         torch.distributed.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------- decode
+
+REPLAYS_LONG = 5     # distinct length / T / index draws cycled through the long-skewed replays
+
+
+def roofline_of(flops: float, nbytes: float, seconds: float, peaks: dict) -> dict:
+    """The roof that binds: max(bytes / HBM peak, FLOPs / bf16 tensor peak).  The
+    kernel is timed per launch (about a millisecond), so the burst tensor peak is
+    the denominator."""
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    tf = flops / seconds / 1e12
+    gbs = nbytes / seconds / 1e9
+    out = {"tensor_achieved_tflops": tf, "tensor_frac": tf / peaks["bf16_tflops"],
+           "hbm_achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+           "t_hbm_us": 1e6 * t_hbm, "t_tensor_us": 1e6 * t_tc}
+    if t_tc >= t_hbm:
+        out.update(bound="tensor", achieved=tf, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                   frac=tf / peaks["bf16_tflops"])
+    else:
+        out.update(bound="hbm", achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s",
+                   frac=gbs / peaks["hbm_gbs"])
+    return out
+
+
+def _timing_events(torch):
+    """Timing events that can be recorded inside a captured graph (event record
+    nodes); None where this torch has no external events."""
+    try:
+        return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
+    except TypeError:
+        return None
+
+
+def decode_main(args, rank: int, world: int):
+    import torch
+    import token_mla_paged_gb300 as m
+
+    if world > 1:
+        import torch.distributed as dist
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev_index = torch.cuda.current_device()
+
+    w, extra = build_workload(args.config)
+    shards = extra["shards"]
+    algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
+    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+    # The draft block has 32 row groups of 128 KV tiles; 64 workers (two splits
+    # each, one item per cluster) measured fastest in a sweep of worker counts.
+    tuned = {"draft_block_bf16": 64} if algo == m.MLA_ALGO_TENSOR else {}
+    workers = args.workers or tuned.get(args.config) or m.default_workers_for(
+        algo, w.batch, w.num_heads, int(w.q_lens().max()), dev_index)
+    # Long skewed contexts: every replay brings new lengths, T and indices (the
+    # persistent kernel re-plans from them); the other workloads replay one batch.
+    replays = [w]
+    if args.config == "long_skewed_fp8":
+        slots = mi.long_skewed_pool_slots(REPLAYS_LONG)
+        w = mi.long_skewed_fp8(replay=0, num_slots=slots)
+        replays = [w] + [mi.long_skewed_fp8(replay=r, num_slots=slots, draw_pool=False)
+                         for r in range(1, REPLAYS_LONG)]
+    maxq = max(int(x.q_lens().max()) for x in replays)
+    runner = m.DecodeRunner(w.batch, w.num_heads, maxq, mode=extra["mode"], num_workers=workers,
+                            kv_len_cap=extra["cap"])
+    if extra["mode"] == m.MLA_PLAN_STATIC:
+        runner.set_host_plan(None, w.qo_indptr)
+    elif extra["mode"] == m.MLA_PLAN_HOST:
+        runner.set_host_plan(w.kv_indptr, w.qo_indptr)
+    dev = mi.to_device(w)
+    # capacity buffers, so every replay's inputs fit the captured graph's pointers
+    max_q = max(x.total_q for x in replays)
+    max_nnz = max(int(x.kv_indptr[-1]) for x in replays)
+    if len(replays) > 1:
+        q_cap = torch.zeros(max_q, w.num_heads, 576, dtype=torch.bfloat16, device="cuda")
+        idx_cap = torch.zeros(max_nnz, dtype=torch.int32, device="cuda")
+        dev["q"], dev["kv_indices"] = q_cap, idx_cap
+
+    def load(x):
+        dev["q"][: x.total_q].copy_(torch.from_numpy(x.q_bits.view(np.int16)).view(torch.bfloat16))
+        dev["kv_indices"][: x.kv_indices.shape[0]].copy_(torch.from_numpy(x.kv_indices))
+        dev["kv_indptr"].copy_(torch.from_numpy(x.kv_indptr))
+        dev["qo_indptr"].copy_(torch.from_numpy(x.qo_indptr))
+
+    load(w)
+    out_fp32 = shards is not None
+    o = torch.empty(max_q, w.num_heads, 512, device="cuda", dtype=torch.float32 if out_fp32 else torch.bfloat16)
+    lse = torch.empty(max_q, w.num_heads, device="cuda", dtype=torch.float32)
+    if shards is not None:
+        R = shards.full.total_q * shards.full.num_heads
+        om = torch.empty(R, 512, dtype=torch.bfloat16, device="cuda")
+        lm = torch.empty(R, dtype=torch.float32, device="cuda")
+
+    def decode():
+        runner.forward(o=o, lse=lse, algo=algo, **dev)
+
+    def merge():
+        if shards is not None:
+            m.mla_merge_states(o.view(shards.num_shards, R, 512), lse.view(shards.num_shards, R), om, lm)
+
+    def step():
+        decode()
+        merge()
+
+    launches_per_step = 1 + (1 if extra["mode"] == m.MLA_PLAN_DYNAMIC else 0) + (1 if shards else 0)
+    flush = L2Flush(torch)
+    full_w = [shards.full] if shards else replays
+    units = [visible_pairs(x) for x in full_w]
+    flops = [FLOP_PER_PAIR * u for u in units]
+    nbytes = [algorithmic_bytes(x) for x in (replays if not shards else [w])]
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    code, info = m.mla_get_device_error(runner.workspace)
+    assert code == 0, f"device error {code} ({info})"
+
+    # One captured graph per step: [event, decode call, event, merge, event].  The
+    # events are record nodes inside the graph, so they bracket device work only.
+    evs = _timing_events(torch)
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap_stream):
+        step()
+    cap_stream.synchronize()
+    with torch.cuda.graph(graph, stream=cap_stream):
+        if evs:
+            evs[0].record()
+        decode()
+        if evs:
+            evs[1].record()
+        merge()
+        if evs:
+            evs[2].record()
+    if evs is None:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        outside = True
+    else:
+        outside = False
+    stream = torch.cuda.current_stream()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_ms, dec_ms, which = [], [], []
+    with ClockSampler(dev_index) as clk:
+        for i in range(args.steps):
+            r = i % len(replays)
+            if len(replays) > 1:
+                load(replays[r])          # new lengths, T and indices (not timed)
+            flush()                       # L2 flush between timed steps (not timed)
+            if outside:
+                evs[0].record(stream)
+            graph.replay()
+            if outside:
+                evs[2].record(stream)
+            torch.cuda.synchronize()
+            step_ms.append(evs[0].elapsed_time(evs[2]))
+            dec_ms.append(evs[0].elapsed_time(evs[1]) if not outside else step_ms[-1])
+            which.append(r)
+    code, info = m.mla_get_device_error(runner.workspace)
+    assert code == 0, f"device error {code} ({info})"
+    if world > 1:
+        torch.distributed.barrier()
+    rates = [units[r % len(units)] / (t * 1e-3) for t, r in zip(step_ms, which)]
+    rate_med = statistics.median(rates)
+    ms_med = statistics.median(step_ms)
+    ms_max = slowest_rank_ms(ms_med, world, device="cuda")
+    rate_job = rate_med * world * ms_med / ms_max      # weak scaling at the slowest rank's time
+    dec_tf = [flops[r % len(flops)] / (t * 1e-3) for t, r in zip(dec_ms, which)]
+    dec_med_ms = statistics.median(dec_ms)
+    k_med = sorted(range(len(dec_tf)), key=lambda k: dec_tf[k])[len(dec_tf) // 2]
+    r_med = which[k_med]
+
+    # End to end through the public API: host (pinned) q + index lists in, O + LSE out.
+    load(w)
+    q_h = dev["q"][: w.total_q].cpu().pin_memory()
+    idx_h = {k: dev[k][: (w.kv_indices.shape[0] if k == "kv_indices" else None)].cpu().pin_memory()
+             for k in ("kv_indptr", "kv_indices", "qo_indptr")}
+    out_final = (om, lm) if shards is not None else (o[: w.total_q], lse[: w.total_q])
+    o_h = torch.empty_like(out_final[0], device="cpu").pin_memory()
+    l_h = torch.empty_like(out_final[1], device="cpu").pin_memory()
+    h2d = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in idx_h.values())
+    host_plan = extra["mode"] == m.MLA_PLAN_HOST
+    if host_plan:
+        kvp_np, qop_np = w.kv_indptr.copy(), w.qo_indptr.copy()
+        plan_h = torch.empty_like(runner.plan_d, device="cpu").pin_memory()
+        h2d += plan_h.numel() * 4
+    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush()
+        e2e_ev[i][0].record(stream)
+        dev["q"][: w.total_q].copy_(q_h, non_blocking=True)
+        for k, t in idx_h.items():
+            dev[k][: t.shape[0]].copy_(t, non_blocking=True)
+        if host_plan:
+            # (every step rebuilds the same bytes, so refilling the pinned buffer
+            # while the previous step's copy may still be queued is harmless)
+            plan_h.numpy()[:] = m.mla_decode_plan(runner.params, kvp_np, qop_np)
+            runner.plan_d.copy_(plan_h, non_blocking=True)
+        step()
+        o_h.copy_(out_final[0], non_blocking=True)
+        l_h.copy_(out_final[1], non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = slowest_rank_ms(statistics.median(a.elapsed_time(b) for a, b in e2e_ev), world, device="cuda")
+
+    peaks = load_peaks()
+    roof = roofline_of(flops[r_med % len(flops)], nbytes[r_med % len(nbytes)], dec_ms[k_med] * 1e-3, peaks)
+    roof.update(traffic=ncu_traffic(args.config) if args.algo == "tensor" else None,
+                peak_source=peaks["source"], alg_flops=flops[r_med % len(flops)],
+                alg_bytes=nbytes[r_med % len(nbytes)],
+                kernel="mla_decode_fwd call (" + ("device planner + " if extra["mode"] == m.MLA_PLAN_DYNAMIC
+                                                   else "") + "decode kernel)",
+                kernel_us_median=1e3 * dec_med_ms)
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            u, s, done, cores = oracle_sample(w, shards, budget_s=12.0)
+            cpu = {"value": u / s, "unit": "KV-tokens*heads/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{done} whole request(s) of the same workload, {s:.1f} s"}
+        line = {
+            "metric": METRIC, "value": rate_job, "unit": "KV-tokens*heads/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-kv/bf16-mma",
+            "data": "synthetic",
+            "config": {"workload": args.config, "batch": w.batch, "heads": w.num_heads,
+                       "q_len": maxq, "kv_tokens": int(w.kv_indptr[-1]),
+                       "kv_dtype": w.kv_dtype, "causal": w.causal,
+                       "plan": ("static", "dynamic", "host")[extra["mode"]],
+                       "algo": args.algo, "workers": workers, "l2": L2_NOTE,
+                       "timing": f"median of {args.steps} CUDA-graph replays"
+                                 + (f", cycling {len(replays)} draws of lengths/T/indices"
+                                    if len(replays) > 1 else "")},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": whole_job_rate(units[0], world, e2e_ms), "unit": "KV-tokens*heads/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="draft_block_bf16",
+    ap.add_argument("--config", default="cp_shards_bf16",
                     choices=mi.CONFIG_NAMES + mi.SPARSE_CONFIG_NAMES + mi.EXTRA_CONFIG_NAMES)
     ap.add_argument("--algo", default="tensor", choices=["tensor", "cuda_core"])
     ap.add_argument("--workers", type=int, default=0, help="plan workers (0 = kernel default)")
@@ -746,151 +998,7 @@ def main():
         print(json.dumps(line))
         return
 
-    import torch
-    import token_mla_paged_gb300 as m
-
-    if world > 1:
-        import torch.distributed as dist
-        local = int(os.environ.get("LOCAL_RANK", "0"))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev_index = torch.cuda.current_device()
-
-    w, extra = build_workload(args.config)
-    shards = extra["shards"]
-    algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
-    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
-    # Plan workers: the tensor kernel runs one item per CTA pair.  The draft block
-    # has 64 row groups, and 64 workers (one item per cluster, no splits) measured
-    # fastest in a sweep of worker counts; the other workloads use one worker per
-    # cluster of the GPU.
-    tuned = {"draft_block_bf16": 64}
-    workers = args.workers or (tuned.get(args.config, sms // 2) if algo == m.MLA_ALGO_TENSOR else sms)
-    maxq = int(w.q_lens().max())
-    runner = m.DecodeRunner(w.batch, w.num_heads, maxq, mode=extra["mode"], num_workers=workers,
-                            kv_len_cap=extra["cap"])
-    if extra["mode"] == m.MLA_PLAN_STATIC:
-        runner.set_host_plan(None, w.qo_indptr)
-    elif extra["mode"] == m.MLA_PLAN_HOST:
-        runner.set_host_plan(w.kv_indptr, w.qo_indptr)
-    dev = mi.to_device(w)
-    out_fp32 = shards is not None
-    o = torch.empty(w.total_q, w.num_heads, 512, device="cuda",
-                    dtype=torch.float32 if out_fp32 else torch.bfloat16)
-    lse = torch.empty(w.total_q, w.num_heads, device="cuda", dtype=torch.float32)
-    if shards is not None:
-        R = shards.full.total_q * shards.full.num_heads
-        om = torch.empty(R, 512, dtype=torch.bfloat16, device="cuda")
-        lm = torch.empty(R, dtype=torch.float32, device="cuda")
-    stream = torch.cuda.current_stream()
-
-    def step():
-        runner.forward(o=o, lse=lse, algo=algo, **dev)
-        if shards is not None:
-            m.mla_merge_states(o.view(shards.num_shards, R, 512), lse.view(shards.num_shards, R), om, lm)
-
-    launches_per_step = 1 + (1 if extra["mode"] == m.MLA_PLAN_DYNAMIC else 0) + (1 if shards else 0)
-    flush = L2Flush(torch)
-    units = visible_pairs(shards.full if shards else w)
-    flops = FLOP_PER_PAIR * units
-    nbytes = algorithmic_bytes(w)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    code, info = m.mla_get_device_error(runner.workspace)
-    assert code == 0, f"device error {code} ({info})"
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev_index) as clk:
-        queue_ahead(torch, args.steps)
-        for i in range(args.steps):
-            flush()                        # L2 flush between timed steps (not timed)
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    times = [a.elapsed_time(b) for a, b in evs]
-    ms = sum(times) / len(times)
-    ms_max = slowest_rank_ms(ms, world, device="cuda")
-
-    # End to end through the public API: host (pinned) q + index lists in, O + LSE out.
-    q_h = dev["q"].cpu().pin_memory()
-    idx_h = {k: dev[k].cpu().pin_memory() for k in ("kv_indptr", "kv_indices", "qo_indptr")}
-    out_final = (om, lm) if shards is not None else (o, lse)
-    o_h = torch.empty_like(out_final[0], device="cpu").pin_memory()
-    l_h = torch.empty_like(out_final[1], device="cpu").pin_memory()
-    h2d = q_h.numel() * q_h.element_size() + sum(t.numel() * 4 for t in idx_h.values())
-    # a HOST plan follows the step's lengths: built on the host and uploaded every step
-    host_plan = extra["mode"] == m.MLA_PLAN_HOST
-    if host_plan:
-        kvp_np, qop_np = w.kv_indptr.copy(), w.qo_indptr.copy()
-        plan_h = torch.empty_like(runner.plan_d, device="cpu").pin_memory()
-        h2d += plan_h.numel() * 4
-    d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush()
-        e2e_ev[i][0].record(stream)
-        dev["q"].copy_(q_h, non_blocking=True)
-        for k, t in idx_h.items():
-            dev[k].copy_(t, non_blocking=True)
-        if host_plan:
-            # (every step rebuilds the same bytes, so refilling the pinned buffer
-            # while the previous step's copy may still be queued is harmless)
-            plan_h.numpy()[:] = m.mla_decode_plan(runner.params, kvp_np, qop_np)
-            runner.plan_d.copy_(plan_h, non_blocking=True)
-        step()
-        o_h.copy_(out_final[0], non_blocking=True)
-        l_h.copy_(out_final[1], non_blocking=True)
-        e2e_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps, world, device="cuda")
-
-    peaks = load_peaks()
-    achieved_tf = flops / (ms * 1e-3) / 1e12
-    achieved_gbs = nbytes / (ms * 1e-3) / 1e9
-    line = None
-    if rank == 0:
-        cpu = None
-        if not args.no_cpu_baseline and world == 1:
-            u, s, done, cores = oracle_sample(w, shards, budget_s=12.0)
-            cpu = {"value": u / s, "unit": "KV-tokens*heads/s", "cores": cores, "kind": "oracle",
-                   "sample": f"{done} whole request(s) of the same workload, {s:.1f} s"}
-        line = {
-            "metric": METRIC, "value": whole_job_rate(units, world, ms_max), "unit": "KV-tokens*heads/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if w.kv_dtype == "bf16" else "fp8-kv/bf16-mma",
-            "data": "synthetic",
-            "config": {"workload": args.config, "batch": w.batch, "heads": w.num_heads,
-                       "q_len": int(w.q_lens().max()), "kv_tokens": int(w.kv_indptr[-1]),
-                       "kv_dtype": w.kv_dtype, "causal": w.causal, "plan": ("static", "dynamic", "host")[extra["mode"]],
-                       "algo": args.algo, "workers": workers, "l2": L2_NOTE},
-            "roofline": {"bound": "tensor", "achieved": achieved_tf, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved_tf / peaks["bf16_tflops"],
-                         "traffic": ncu_traffic(args.config) if args.algo == "tensor" else None,
-                         "peak_source": peaks["source"], "hbm_achieved_gbs": achieved_gbs,
-                         "hbm_frac": achieved_gbs / peaks["hbm_gbs"], "alg_flops": flops,
-                         "alg_bytes": nbytes},
-            "cpu_baseline": cpu,
-            "e2e": {"value": whole_job_rate(units, world, e2e_ms), "unit": "KV-tokens*heads/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
-        }
-        print(json.dumps(line))
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    return decode_main(args, rank, world)
 
 
 if __name__ == "__main__":

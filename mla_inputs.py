@@ -122,8 +122,12 @@ def _indptr(lens) -> np.ndarray:
 def make_workload(name: str, *, batch: int, num_heads: int, q_lens, kv_lens,
                   kv_dtype: str, causal: bool, seed: int, num_slots: Optional[int] = None,
                   softmax_scale: float = SOFTMAX_SCALE, kv_scale: Optional[float] = None,
-                  identical_q_rows: bool = False) -> Workload:
-    """Generic generator: random q, random pool, kv_indices = seeded permutation prefix."""
+                  identical_q_rows: bool = False, draw_pool: bool = True) -> Workload:
+    """Generic generator: random q, random pool, kv_indices = seeded permutation prefix.
+
+    ``draw_pool=False`` leaves the pool undrawn (an all-zero read-only view of the
+    right shape): for extra draws of lengths and indices that reuse another
+    workload's pool."""
     rng = np.random.default_rng(seed)
     q_lens = np.asarray(q_lens, dtype=np.int64)
     kv_lens = np.asarray(kv_lens, dtype=np.int64)
@@ -143,7 +147,11 @@ def make_workload(name: str, *, batch: int, num_heads: int, q_lens, kv_lens,
     else:
         qf = rng.standard_normal((total_q, num_heads, D_QK), dtype=np.float32)
     q_bits = to_bf16_bits(qf)
-    kv_bits = _normal_bits(rng, (num_slots, D_QK), kv_dtype, kv_scale)
+    if draw_pool:
+        kv_bits = _normal_bits(rng, (num_slots, D_QK), kv_dtype, kv_scale)
+    else:
+        kv_bits = np.broadcast_to(np.zeros((1, D_QK), dtype=np.uint16 if kv_dtype == "bf16" else np.uint8),
+                                  (num_slots, D_QK))
     return Workload(name=name, num_heads=num_heads, q_bits=q_bits, kv_bits=kv_bits,
                     kv_dtype=kv_dtype, kv_indptr=_indptr(kv_lens), kv_indices=kv_indices,
                     qo_indptr=_indptr(q_lens), causal=causal, softmax_scale=softmax_scale,
@@ -193,7 +201,7 @@ def verify_fp8(scale: float = 1.0, seed: Optional[int] = None) -> Workload:
 
 
 def long_skewed_fp8(replay: int = 0, scale: float = 1.0, num_slots: Optional[int] = None,
-                    batch: int = 64) -> Workload:
+                    batch: int = 64, draw_pool: bool = True) -> Workload:
     """Batch 64, T in {1,2,4}, 128 heads, fp8, L = floor(exp(U[ln 256, ln 131072])), causal.
 
     ``replay`` selects a fresh draw of lengths, T and indices (graph replays with
@@ -206,7 +214,8 @@ def long_skewed_fp8(replay: int = 0, scale: float = 1.0, num_slots: Optional[int
     qls = rng.choice(np.array([1, 2, 4]), size=batch)
     w = make_workload("long_skewed_fp8" + ("" if scale == 1.0 else f"_x{scale:g}") + f"_r{replay}",
                       batch=batch, num_heads=128, q_lens=qls, kv_lens=lens, kv_dtype="fp8",
-                      causal=True, seed=int(rng.integers(1 << 31)), num_slots=num_slots)
+                      causal=True, seed=int(rng.integers(1 << 31)), num_slots=num_slots,
+                      draw_pool=draw_pool)
     return w
 
 

@@ -22,8 +22,8 @@ if not torch.cuda.is_available():  # pragma: no cover
 import token_mla_paged_gb300 as m  # noqa: E402
 
 
-def _capacity_buffers(ws, B, H, max_T, num_slots):
-    max_nnz = max(int(w.kv_indptr[-1]) for w in ws)
+def _capacity_buffers(B, H, max_T, num_slots):
+    max_nnz = num_slots            # every replay's index list fits the pool
     max_q = B * max_T
     dev = dict(
         q=torch.zeros(max_q, H, 576, dtype=torch.bfloat16, device="cuda"),
@@ -48,18 +48,19 @@ def _load(dev, w):
 def test_graph_replay_with_changing_lengths(algo, scale):
     if algo == m.MLA_ALGO_CUDA_CORE and scale == 1.0:
         pytest.skip("full-size replays checked on the tensor kernel")
-    replays = 5 if scale < 1 else 2
+    replays = 5
     slots = mi.long_skewed_pool_slots(replays, scale=scale)
-    ws = [mi.long_skewed_fp8(replay=r, scale=scale, num_slots=slots) for r in range(replays)]
-    # each replay brings fresh lengths, T, indices and cache contents (pool sized for all)
-    B, H = ws[0].batch, ws[0].num_heads
-    dev, o, lse = _capacity_buffers(ws, B, H, 4, slots)
+    # each replay brings fresh lengths, T, indices and cache contents (pool sized for
+    # all); the workloads are drawn one at a time to bound host memory
+    w0 = mi.long_skewed_fp8(replay=0, scale=scale, num_slots=slots)
+    B, H = w0.batch, w0.num_heads
+    dev, o, lse = _capacity_buffers(B, H, 4, slots)
     pool = torch.zeros(slots, 576, dtype=torch.uint8, device="cuda")
     runner = m.DecodeRunner(B, H, 4, mode=m.MLA_PLAN_DYNAMIC, num_workers=76)
     kw = dict(kv_pool=pool.view(torch.float8_e4m3fn), kv_dtype=m.MLA_KV_FP8_E4M3, causal=True,
-              softmax_scale=ws[0].softmax_scale, kv_scale=ws[0].kv_scale)
-    _load(dev, ws[0])
-    pool.copy_(torch.from_numpy(ws[0].kv_bits))
+              softmax_scale=w0.softmax_scale, kv_scale=w0.kv_scale)
+    _load(dev, w0)
+    pool.copy_(torch.from_numpy(w0.kv_bits))
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         runner.forward(o=o, lse=lse, algo=algo, **dev, **kw)       # warm-up outside capture
@@ -68,7 +69,8 @@ def test_graph_replay_with_changing_lengths(algo, scale):
     with torch.cuda.graph(graph, stream=stream):
         runner.forward(o=o, lse=lse, algo=algo, **dev, **kw)
     outs = []
-    for r, w in enumerate(ws):
+    for r in range(replays):
+        w = w0 if r == 0 else mi.long_skewed_fp8(replay=r, scale=scale, num_slots=slots)
         _load(dev, w)
         pool.copy_(torch.from_numpy(w.kv_bits))
         torch.cuda.synchronize()
@@ -85,6 +87,5 @@ def test_graph_replay_with_changing_lengths(algo, scale):
     # replaying the last lengths again gives bitwise the same result
     graph.replay()
     torch.cuda.synchronize()
-    w = ws[-1]
     assert np.array_equal(o[: w.total_q].double().cpu().numpy(), outs[-1][0])
     assert np.array_equal(lse[: w.total_q].double().cpu().numpy(), outs[-1][1])

@@ -21,15 +21,9 @@ if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skippe
 
 import token_mla_paged_gb300 as m  # noqa: E402
 
-ALGOS = [m.MLA_ALGO_CUDA_CORE]
-try:
-    _probe = m.DecodeRunner(1, 16, 1)
-    w0 = mi.make_workload("probe", batch=1, num_heads=16, q_lens=[1], kv_lens=[4], kv_dtype="bf16",
-                          causal=False, seed=1, num_slots=8)
-    hz.run(w0, algo=m.MLA_ALGO_TENSOR, runner=_probe)
-    ALGOS.append(m.MLA_ALGO_TENSOR)
-except m.MlaError:
-    pass
+# Both kernels are always in the matrix: on an sm_103a device a tensor-kernel
+# launch failure fails these tests instead of dropping the kernel from them.
+ALGOS = [m.MLA_ALGO_CUDA_CORE, m.MLA_ALGO_TENSOR]
 ALGO_IDS = {m.MLA_ALGO_CUDA_CORE: "cuda_core", m.MLA_ALGO_TENSOR: "tensor"}
 
 

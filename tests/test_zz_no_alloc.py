@@ -4,10 +4,10 @@ Some callers of this library cannot allocate device memory themselves: a
 framework or runtime that owns the device allocator and hands the kernel only
 its input and output tensors.  For them the library keeps its plan buffer and
 workspace in one static device array.  This test calls that entry point through
-the C ABI and checks its output against the regular entry point (which uses a
-caller-allocated plan and workspace) on the same inputs, within the parity
-tolerance of the other GPU tests, on two calls in a row (the second call sees
-the first call's leftovers in the shared array).
+the C ABI and checks its output against the float64 oracle and against the
+regular entry point (which uses a caller-allocated plan and workspace) on the
+same inputs, within the parity tolerance of the other GPU tests, on two calls in
+a row (the second call sees the first call's leftovers in the shared array).
 
 The file is named so that pytest collects it last.
 """
@@ -17,6 +17,7 @@ import numpy as np
 import pytest
 
 import mla_inputs as mi
+from oracle import mla_oracle as mo
 
 pytestmark = pytest.mark.gpu
 
@@ -66,6 +67,8 @@ def test_noalloc_matches_regular_entry_point(kv_dtype):
     H = w.num_heads
     # regular entry point: caller-owned plan and workspace
     O_ref, L_ref, _ = hz.run(w, algo=m.MLA_ALGO_TENSOR, mode=m.MLA_PLAN_DYNAMIC, num_workers=24, dev=dev)
+    O_or, L_or = mo.mla_decode_workload(w)
+    hz.assert_close(O_ref, L_ref, O_or, L_or, kv_dtype, what="regular entry point")
     params = m.plan_params(w.batch, H, int(w.q_lens().max()), 24, 0, m.MLA_PLAN_DYNAMIC)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
@@ -76,7 +79,8 @@ def test_noalloc_matches_regular_entry_point(kv_dtype):
         torch.cuda.synchronize()
         O = o.double().cpu().numpy()
         L = lse.double().cpu().numpy()
-        hz.assert_close(O, L, O_ref, L_ref, kv_dtype, what=f"noalloc call {call}")
+        hz.assert_close(O, L, O_or, L_or, kv_dtype, what=f"noalloc call {call} vs oracle")
+        hz.assert_close(O, L, O_ref, L_ref, kv_dtype, what=f"noalloc call {call} vs regular entry point")
 
 
 def test_noalloc_rejects_static_mode_and_oversized_problems():

@@ -305,7 +305,7 @@ def mla_get_device_error(workspace_d, stream=None) -> Tuple[int, int]:
     return code.value, info.value
 
 
-from .runner import DecodeRunner  # noqa: E402  (plumbing: buffers + calls, no compute)
+from .runner import DecodeRunner, default_workers_for  # noqa: E402  (plumbing: buffers + calls, no compute)
 
 
 def mla_absorb_bmm(x, w, out, w_scale: float = 1.0, status=None, stream=None) -> None:

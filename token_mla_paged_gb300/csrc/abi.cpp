@@ -25,6 +25,27 @@ bool aligned(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
 
 }  // namespace
 
+namespace mla {
+
+int current_device_slot() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+int device_sm_count(int dev) {
+  static int sms[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+}  // namespace mla
+
 extern "C" {
 
 int mla_abi_version(void) { return MLA_ABI_VERSION; }

@@ -372,20 +372,13 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-int sm_count() {
-  static int n[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (!n[dev] && cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n[dev] = 0;
-  return n[dev];
-}
-
 }  // namespace
 
 mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
   if (a.num_tokens == 0) return MLA_OK;
   EncodeTiledFn enc = encoder();
-  const int sms = sm_count();
+  const int dev = current_device_slot();
+  const int sms = device_sm_count(dev);
   if (!enc || sms <= 0) return MLA_ERR_CUDA;
   const bool fp8 = a.w_dtype == MLA_W_FP8_E4M3;
 
@@ -443,12 +436,12 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
   const int grid = p.units < sms ? p.units : sms;
   // The shared-memory limit is raised once per kernel (to the largest size any
   // call needs), outside stream capture in the usual first-call-then-capture order.
-  static int smem_set[2] = {0, 0};
+  static int smem_set[kMaxDevices][2] = {};
   auto kern = fp8 ? mla_absorb_bmm_kernel<true> : mla_absorb_bmm_kernel<false>;
-  if (smem > smem_set[fp8]) {
+  if (smem > smem_set[dev][fp8]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return MLA_ERR_CUDA;
-    smem_set[fp8] = smem;
+    smem_set[dev][fp8] = smem;
   }
   kern<<<grid, threads_for(fp8), smem, (cudaStream_t)stream>>>(tx, tw, p);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

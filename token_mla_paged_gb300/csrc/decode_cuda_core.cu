@@ -229,26 +229,21 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_cuda_core_kernel(Decod
   }
 }
 
-int g_num_sms = 0;
-
 }  // namespace
 
 mla_status launch_decode_cuda_core(const DecodeParams& dp, void* stream) {
   const size_t smem = sizeof(float) * (size_t)(kSubRows * kStride + kTile * kStride + kSubRows * (kTile + 1));
-  static bool attr_done = false;
-  if (!attr_done) {
+  static bool attr_done[kMaxDevices] = {false};
+  const int dev = current_device_slot();
+  const int num_sms = device_sm_count(dev);
+  if (num_sms == 0) return MLA_ERR_CUDA;
+  if (!attr_done[dev]) {
     if (cudaFuncSetAttribute(mla_decode_cuda_core_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return MLA_ERR_CUDA;
-    attr_done = true;
+    attr_done[dev] = true;
   }
-  if (g_num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return MLA_ERR_CUDA;
-  }
-  mla_decode_cuda_core_kernel<<<g_num_sms, kThreads, smem, (cudaStream_t)stream>>>(dp);
+  mla_decode_cuda_core_kernel<<<num_sms, kThreads, smem, (cudaStream_t)stream>>>(dp);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -866,9 +866,10 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
   if (cr != CUDA_SUCCESS) return MLA_ERR_INVALID_ARG;
   const int smem = kSmemBytes + kSmemAlign;
   auto kern = mla_decode_tensor_kernel<kFp8>;
-  static int configured[2] = {0, 0};
-  static int max_clusters[2] = {0, 0};
-  if (!configured[kFp8]) {
+  static int max_clusters[kMaxDevices][2] = {};
+  const int dev = current_device_slot();
+  if (dev < 0) return MLA_ERR_CUDA;
+  if (max_clusters[dev][kFp8] == 0) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return MLA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -884,10 +885,9 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
     cfg.numAttrs = 1;
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
-    max_clusters[kFp8] = n;
-    configured[kFp8] = 1;
+    max_clusters[dev][kFp8] = n;
   }
-  int clusters = max_clusters[kFp8];
+  int clusters = max_clusters[dev][kFp8];
   if (clusters > dp.items_cap) clusters = dp.items_cap > 0 ? dp.items_cap : 1;
   DecodeParams kp = dp;
   if (kFp8) {

@@ -5,8 +5,9 @@
 //
 //   M = max_s LSE_s;  LSE = M + ln sum_s exp(LSE_s - M);  O = sum_s exp(LSE_s - LSE) O_s
 //
-// One warp per row; lanes stride over the row's dv columns (coalesced), and the
-// per-state weights are computed once per row and broadcast with shuffles.
+// One warp per row; lanes stride over the row's dv columns (coalesced).  For up
+// to 32 states the per-state weights are computed once per row (one per lane)
+// and broadcast with shuffles; more states recompute them per column block.
 // The work is HBM-bound: n*dv reads and dv writes per row.
 #include <cuda_runtime.h>
 
@@ -37,15 +38,28 @@ mla_merge_states_kernel(const void* __restrict__ o_parts, int parts_fp32,
       for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
     }
     const float inv_tot = M != -INFINITY ? 1.f / tot : 0.f;
+    // Weight of state s: exp(LSE_s - M) / tot.  With n <= 32 lane s keeps state
+    // s's weight in a register for the whole row; beyond that the weights of each
+    // 32-state chunk are recomputed per column block.  Either way the states are
+    // summed in order 0..n-1 for every column.
+    const bool hoisted = n <= 32;
+    float w_own = 0.f;
+    if (hoisted && lane < n && M != -INFINITY) {
+      const float ls = lse_parts[(int64_t)lane * rows + r];
+      w_own = ls == -INFINITY ? 0.f : exp2f((ls - M) * 1.4426950408889634f) * inv_tot;
+    }
     for (int d0 = 0; d0 < dv; d0 += 32) {
       const int d = d0 + lane;
       float acc = 0.f;
       if (M != -INFINITY) {
         for (int c = 0; c < n; c += 32) {
-          float w = 0.f;
-          if (c + lane < n) {
-            const float ls = lse_parts[(int64_t)(c + lane) * rows + r];
-            w = ls == -INFINITY ? 0.f : exp2f((ls - M) * 1.4426950408889634f) * inv_tot;
+          float w = w_own;
+          if (!hoisted) {
+            w = 0.f;
+            if (c + lane < n) {
+              const float ls = lse_parts[(int64_t)(c + lane) * rows + r];
+              w = ls == -INFINITY ? 0.f : exp2f((ls - M) * 1.4426950408889634f) * inv_tot;
+            }
           }
           const int cnt = min(32, n - c);
           for (int k = 0; k < cnt; ++k) {
@@ -73,13 +87,8 @@ mla_merge_states_kernel(const void* __restrict__ o_parts, int parts_fp32,
 mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const float* lse_parts,
                                int n, int64_t rows, int dv, void* o, int o_fp32, float* lse,
                                void* stream) {
-  static int num_sms = 0;
-  if (num_sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    if (cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return MLA_ERR_CUDA;
-  }
+  const int num_sms = device_sm_count(current_device_slot());
+  if (num_sms == 0) return MLA_ERR_CUDA;
   const int64_t want = (rows + 7) / 8;
   const int grid = (int)(want < (int64_t)num_sms * 16 ? want : (int64_t)num_sms * 16);
   mla_merge_states_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>(

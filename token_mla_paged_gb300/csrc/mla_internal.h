@@ -121,4 +121,13 @@ mla_status launch_rope_q_cache(const mla_rope_q_cache_args& a, void* stream);
 mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream);
 int tensor_kernel_available();
 
+// Launch-time facts cached per device (opt-in shared-memory sizes, SM counts,
+// occupancy): cudaFuncSetAttribute and the SM count belong to one device, so the
+// launchers keep one entry per device index.  Returns the current device index,
+// or -1 if it cannot be read or is >= kMaxDevices.  Two host threads that fill
+// the same entry at once write the same values.
+constexpr int kMaxDevices = 64;
+int current_device_slot();
+int device_sm_count(int dev);   // 0 on error
+
 }  // namespace mla

@@ -24,7 +24,6 @@ namespace mla {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -212,12 +212,14 @@ mla_status launch_plan_device(const mla_plan_params& p, const int32_t* kv_indptr
   int p2cap = 1;
   while (p2cap < g.items_cap) p2cap <<= 1;
   const size_t smem = sizeof(int) * (6 * (size_t)(p.batch + 1) + (size_t)p2cap);
-  static size_t attr_set = 0;
-  if (smem > 48 * 1024 && smem > attr_set) {
+  static size_t attr_set[kMaxDevices] = {0};
+  const int dev = current_device_slot();
+  if (dev < 0) return MLA_ERR_CUDA;
+  if (smem > 48 * 1024 && smem > attr_set[dev]) {
     if (cudaFuncSetAttribute(mla_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return MLA_ERR_CUDA;
-    attr_set = smem;
+    attr_set[dev] = smem;
   }
   mla_plan_kernel<<<1, kPlanThreads, smem, (cudaStream_t)stream>>>(
       p.batch, p.num_heads, p.max_q_len, p.num_workers, g.items_cap, p2cap, kv_indptr, qo_indptr,

@@ -111,18 +111,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
       "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
       : "memory");
 }
-// Same gather, written to the same shared-memory offset of every CTA in `mask`
-// (bit r = cluster rank r); each destination's barrier at `bar`'s offset gets
-// the bytes that landed there.
-__device__ __forceinline__ void tma_gather4_mc(uint32_t dst, const void* tmap, int32_t col, int32_t r0,
-                                               int32_t r1, int32_t r2, int32_t r3, uint64_t* bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
-      "l"(tmap), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -15,6 +15,13 @@ def default_workers(device=None) -> int:
     return int(torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count)
 
 
+def default_workers_for(algo: int, batch: int, num_heads: int, max_q_len: int, device=None) -> int:
+    """Plan workers for a shape: the tensor kernel runs one work item per CTA
+    pair, so one worker per pair of SMs; the CUDA-core kernel one per SM."""
+    sms = default_workers(device)
+    return sms // 2 if algo == MLA_ALGO_TENSOR else sms
+
+
 class DecodeRunner:
     """Owns one plan buffer and one workspace sized for `params`.
 
