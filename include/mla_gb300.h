@@ -75,11 +75,11 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 4
+#define MLA_ABI_VERSION 5
 #define MLA_D_QK 576             /* latent 512 + RoPE 64 */
 #define MLA_D_V 512
-#define MLA_ROWS_PER_GROUP 128   /* query rows (t,h) handled together */
-#define MLA_BLOCK_N 64           /* KV entries per tile */
+#define MLA_ROWS_PER_GROUP 256   /* query rows (t,h) of one work item */
+#define MLA_BLOCK_N 128          /* KV entries per tile (split granularity) */
 #define MLA_MAX_SPLITS 16
 
 typedef enum {
@@ -186,11 +186,22 @@ typedef struct {
 /* ABI version (MLA_ABI_VERSION); lets a caller probe capabilities by number
  * rather than by inspecting signatures.  3: per-entry positions and the sliding
  * window in mla_fwd_args, HOST plans, mla_cache_write, mla_rope_q_cache;
- * 4: mla_absorb_bmm. */
+ * 4: mla_absorb_bmm; 5: work items of 256 query rows over 128-entry tiles (the
+ * plan layout changed) and mla_decode_workers. */
 int mla_abi_version(void);
 
 /* Static description of a status code; never NULL. */
 const char* mla_status_string(int status);
+
+/* Number of work items the decode kernel of `algo` (mla_algo) runs at once on
+ * the current device: the clusters of the tensor kernel that fit on the GPU
+ * together, or the SMs for the CUDA-core kernel.  The persistent workers a plan
+ * balances its splits over ("[DSV4] Tuned ASM FP8 decode with split plans; HCA
+ * on aiter's persistent V4-NM kernel", Summary part 2); pass it as
+ * mla_plan_params.num_workers.  Host call; queries the device's occupancy once
+ * per device.  MLA_ERR_INVALID_ARG for an unknown algo or NULL out pointer,
+ * MLA_ERR_CUDA if the device cannot be queried. */
+mla_status mla_decode_workers(int32_t algo, int32_t* num_workers);
 
 /* Sizes of the plan buffer and of the device workspace for these params.  Both
  * are upper bounds valid for any lengths the params allow.  Host only. */

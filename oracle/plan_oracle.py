@@ -12,7 +12,10 @@ The pages fix the ideas, not the numbers:
     16-row uniform split table);
   * a persistent kernel that plans the split from the real per-row KV lengths on
     every call ("[DSV4] ...", Summary part 2).
-The constants and the tie-break rules below are this build's choices.
+The constants and the tie-break rules below are this build's choices.  ROWS and
+BLOCK_N are the library's (256 query rows per work item, 128 KV entries per tile);
+every function also takes them as keyword arguments, so plans worked out by hand
+for other values stay checkable.
 
 Specification (all integers, 64-bit intermediates):
   For request b:  T_b = qo_indptr[b+1]-qo_indptr[b],  L_b = kv_indptr[b+1]-kv_indptr[b]
@@ -47,8 +50,8 @@ import numpy as np
 
 MAGIC = 0x4D4C4150
 VERSION = 1
-ROWS = 128
-BLOCK_N = 64
+ROWS = 256
+BLOCK_N = 128
 MAX_SPLITS = 16
 MIN_TILES = 4
 COST_CLAMP = 65535
@@ -62,17 +65,18 @@ def cdiv(a: int, b: int) -> int:
     return -(-a // b)
 
 
-def items_capacity(batch: int, num_heads: int, max_q_len: int, num_workers: int) -> int:
-    return num_workers + batch * cdiv(num_heads * max_q_len, ROWS)
+def items_capacity(batch: int, num_heads: int, max_q_len: int, num_workers: int, rows: int = ROWS) -> int:
+    return num_workers + batch * cdiv(num_heads * max_q_len, rows)
 
 
-def plan_ints(batch: int, num_heads: int, max_q_len: int, num_workers: int) -> int:
-    cap = items_capacity(batch, num_heads, max_q_len, num_workers)
+def plan_ints(batch: int, num_heads: int, max_q_len: int, num_workers: int, rows: int = ROWS) -> int:
+    cap = items_capacity(batch, num_heads, max_q_len, num_workers, rows)
     return HEADER_INTS + batch + (batch + 1) + batch + 4 * cap
 
 
 def build_plan(batch: int, num_heads: int, max_q_len: int, num_workers: int, kv_len_cap: int,
-               mode: int, kv_indptr: Optional[np.ndarray], qo_indptr: np.ndarray) -> np.ndarray:
+               mode: int, kv_indptr: Optional[np.ndarray], qo_indptr: np.ndarray, *,
+               rows: int = ROWS, block_n: int = BLOCK_N) -> np.ndarray:
     """Return the plan buffer as an int32 array (raises ValueError on invalid input)."""
     if batch < 0 or num_heads < 1 or max_q_len < 0 or num_workers < 1 or mode not in (STATIC, DYNAMIC, HOST):
         raise ValueError("invalid plan parameters")
@@ -85,10 +89,10 @@ def build_plan(batch: int, num_heads: int, max_q_len: int, num_workers: int, kv_
         L = [int(kv_indptr[b + 1]) - int(kv_indptr[b]) for b in range(batch)]
         if any(x < 0 for x in L):
             raise ValueError("decreasing kv_indptr")
-        N = [cdiv(x, BLOCK_N) for x in L]
+        N = [cdiv(x, block_n) for x in L]
     else:
-        N = [cdiv(int(kv_len_cap), BLOCK_N)] * batch
-    G = [cdiv(num_heads * t, ROWS) for t in T]
+        N = [cdiv(int(kv_len_cap), block_n)] * batch
+    G = [cdiv(num_heads * t, rows) for t in T]
     total = sum(g * n for g, n in zip(G, N))
     target = max(MIN_TILES, cdiv(total, num_workers))
     S = [min(MAX_SPLITS, max(1, cdiv(n, target))) for n in N]
@@ -115,15 +119,15 @@ def build_plan(batch: int, num_heads: int, max_q_len: int, num_workers: int, kv_
             for g in range(G[b]):
                 slot = partial_base[b] + s * G[b] + g if S[b] > 1 else -1
                 items.append((min(cost, COST_CLAMP), len(items), (b, s, g, slot)))
-    cap = items_capacity(batch, num_heads, max_q_len, num_workers)
+    cap = items_capacity(batch, num_heads, max_q_len, num_workers, rows)
     if len(items) > cap or cap > 65535:
         raise ValueError("item capacity exceeded")
     items.sort(key=lambda it: (-it[0], it[1]))
 
-    out = np.zeros(plan_ints(batch, num_heads, max_q_len, num_workers), dtype=np.int64)
+    out = np.zeros(plan_ints(batch, num_heads, max_q_len, num_workers, rows), dtype=np.int64)
     cap64 = int(kv_len_cap) if mode == STATIC else 0
     hdr = [MAGIC, VERSION, batch, num_heads, max_q_len, num_workers, mode, len(items), n_partials,
-           group_base[batch], cap64 & 0xFFFFFFFF, (cap64 >> 32) & 0xFFFFFFFF, ROWS, BLOCK_N, cap, 0]
+           group_base[batch], cap64 & 0xFFFFFFFF, (cap64 >> 32) & 0xFFFFFFFF, rows, block_n, cap, 0]
     out[:HEADER_INTS] = hdr
     o = HEADER_INTS
     out[o:o + batch] = S
@@ -156,9 +160,9 @@ def parse_plan(buf: np.ndarray) -> dict:
                 splits=S, group_base=gb, partial_base=pb, items=items, capacity=cap)
 
 
-def split_tile_range(s: int, S_b: int, L_b: int):
+def split_tile_range(s: int, S_b: int, L_b: int, block_n: int = BLOCK_N):
     """Entry range [e0, e1) of split s of S_b over a request of real length L_b."""
-    N = cdiv(L_b, BLOCK_N)
+    N = cdiv(L_b, block_n)
     t0 = (s * N) // S_b
     t1 = ((s + 1) * N) // S_b
-    return BLOCK_N * t0, min(BLOCK_N * t1, L_b)
+    return block_n * t0, min(block_n * t1, L_b)

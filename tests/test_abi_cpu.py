@@ -88,9 +88,12 @@ def test_host_plan_for_the_five_workloads():
 def test_plan_sizes_follow_the_bounds():
     p = m.plan_params(64, 128, 4, 76, 0, m.MLA_PLAN_DYNAMIC)
     plan_bytes, ws_bytes = m.mla_decode_plan_size(p)
-    cap = 76 + 64 * 4
+    rows = po.ROWS                       # 256 query rows per item: 128 x 4 rows -> 2 groups
+    g_max = -(-128 * 4 // rows)
+    cap = 76 + 64 * g_max
     assert plan_bytes == 4 * (16 + 64 + 65 + 64 + 4 * cap)
-    assert ws_bytes >= 4 * cap * 128 * 512 + 4 * cap * 128 + 4 * 64 * 4 + 256
+    # partial O and LSE per item, two merge counters (one per row half) per group
+    assert ws_bytes >= 4 * cap * rows * 512 + 4 * cap * rows + 4 * 2 * 64 * g_max + 256
 
 
 def test_host_plan_rejects_bad_input():

@@ -299,7 +299,7 @@ def _check_plan_case(c):
     buf = po.build_plan(c["batch"], c["num_heads"], c["max_q_len"], c["num_workers"],
                         c["kv_len_cap"], c["mode"],
                         None if c["kv_indptr"] is None else np.array(c["kv_indptr"]),
-                        np.array(c["qo_indptr"]))
+                        np.array(c["qo_indptr"]), rows=c["rows"], block_n=c["block_n"])
     p = po.parse_plan(buf)
     assert p["magic"] == po.MAGIC and p["version"] == po.VERSION
     assert list(p["splits"]) == c["splits"]
@@ -361,6 +361,13 @@ def test_plan_properties(seed):
             assert a == e and c >= a
             e = c
         assert e == int(L[b])
+
+
+def test_split_ranges_of_the_256_row_worked_example():
+    """Hand-worked: 4000 entries in 128-entry tiles (32 tiles) split in two."""
+    assert po.split_tile_range(0, 2, 4000, block_n=128) == (0, 2048)
+    assert po.split_tile_range(1, 2, 4000, block_n=128) == (2048, 4000)
+    assert po.split_tile_range(0, 1, 1000, block_n=128) == (0, 1000)
 
 
 def test_plan_rejects_bad_input():

@@ -110,6 +110,7 @@ def _load():
         "mla_rope_q_cache": (ctypes.c_int, [ctypes.POINTER(RopeArgs), vp]),
         "mla_absorb_bmm": (ctypes.c_int, [ctypes.POINTER(BmmArgs), vp]),
         "mla_get_device_error": (ctypes.c_int, [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+        "mla_decode_workers": (ctypes.c_int, [i32, ctypes.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -124,7 +125,7 @@ _lib = _load()
 ABI_SYMBOLS = ("mla_abi_version", "mla_status_string", "mla_decode_plan_size", "mla_decode_plan",
                "mla_decode_plan_device", "mla_decode_fwd", "mla_merge_states",
                "mla_get_device_error", "mla_decode_fwd_noalloc", "mla_cache_write", "mla_rope_q_cache",
-               "mla_absorb_bmm")
+               "mla_absorb_bmm", "mla_decode_workers")
 
 
 def library():
@@ -147,6 +148,13 @@ def mla_status_string(status: int) -> str:
 def plan_params(batch: int, num_heads: int, max_q_len: int, num_workers: int,
                 kv_len_cap: int = 0, mode: int = MLA_PLAN_DYNAMIC) -> PlanParams:
     return PlanParams(batch, num_heads, max_q_len, num_workers, kv_len_cap, mode, 0)
+
+
+def mla_decode_workers(algo: int) -> int:
+    """Work items the decode kernel of `algo` runs at once on the current device."""
+    n = ctypes.c_int32(0)
+    _check(_lib.mla_decode_workers(algo, ctypes.byref(n)), "mla_decode_workers")
+    return int(n.value)
 
 
 def mla_decode_plan_size(params: PlanParams) -> Tuple[int, int]:

@@ -3,6 +3,7 @@
 // allocates device memory, synchronises (except mla_get_device_error) or reads
 // device memory on the host, so the forward path can be captured in a CUDA graph.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include <cuda_runtime.h>
@@ -61,6 +62,14 @@ const char* mla_status_string(int status) {
     case MLA_ERR_DEVICE_FAULT: return "device-side fault recorded in the workspace";
     default: return "unknown status";
   }
+}
+
+mla_status mla_decode_workers(int32_t algo, int32_t* num_workers) {
+  if (!num_workers || (algo != MLA_ALGO_TENSOR && algo != MLA_ALGO_CUDA_CORE)) return MLA_ERR_INVALID_ARG;
+  const int n = algo == MLA_ALGO_TENSOR ? tensor_kernel_workers() : device_sm_count(current_device_slot());
+  if (n < 1) return MLA_ERR_CUDA;
+  *num_workers = n;
+  return MLA_OK;
 }
 
 mla_status mla_decode_plan_size(const mla_plan_params* params, size_t* plan_bytes,
@@ -171,6 +180,16 @@ mla_status mla_decode_fwd(const mla_fwd_args* a, void* stream) {
   dp.o = a->o;
   dp.lse = a->lse;
   dp.plan = (const int32_t*)a->plan_d;
+  dp.wait_limit = 2000000000LL;   // about a second at GB300 clocks
+  // Failure-path test hook (tests only): MLA_TEST_STALL_CYCLES=<n> makes the
+  // tensor kernel wait on a barrier nothing signals, with a limit of n cycles.
+  if (const char* e = std::getenv("MLA_TEST_STALL_CYCLES")) {
+    const long long n = std::atoll(e);
+    if (n > 0) {
+      dp.test_stall = 1;
+      dp.wait_limit = n;
+    }
+  }
   dp.ws_hdr = (int32_t*)ws;
   dp.counters = (int32_t*)(ws + wg.counters_off);
   dp.part_lse = (float*)(ws + wg.part_lse_off);

@@ -3,8 +3,8 @@
 // the tensor-core path and as the simplest correct implementation on sm_103a.
 //
 // Persistent blocks pull work items (request b, split s, row group g) from an
-// atomic queue over the plan's cost-sorted item list.  A 128-row group is
-// processed as four 32-row passes over the item's KV range; each pass keeps
+// atomic queue over the plan's cost-sorted item list.  An item's rows (up to
+// 256) are processed as 32-row passes over the item's KV range; each pass keeps
 // Q[32, 576] and one KV tile [32, 576] in shared memory as fp32, the running
 // max/sum per row in registers and O[32, 512] spread over 256 threads.
 #include <cuda_runtime.h>

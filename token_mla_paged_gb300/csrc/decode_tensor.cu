@@ -1,28 +1,39 @@
-// Tensor-core MLA decode kernel for sm_103a (tcgen05 + TMEM + TMA gathers).
+// Tensor-core MLA decode kernel for sm_103a (tcgen05 pairs + TMEM + TMA gathers).
 //
 // All H*T query rows of a request share one stream of latent KV rows, so QK^T
-// over 576 columns and PV over 512 are dense contractions with M = 128 query
-// rows.  The fp32 accumulator of O[128, 512] alone fills the 512 TMEM columns of
-// an SM, so each work item runs on a cluster of two CTAs with different jobs:
+// over 576 columns and PV over 512 are dense contractions.  A work item is 256
+// query rows of one request (two 128-row halves) over one split of its KV
+// entries, and runs on a cluster of four CTAs on four SMs:
 //
-//   rank 0, the score CTA: holds the item's Q[128, 576] in TMEM as the MMA's A
-//     operand, gathers K tiles [64 entries, 576] with TMA, computes
-//     S = Q K^T into a double-buffered TMEM tile, runs the masked online
-//     softmax (one thread per query row) and ships P (bf16) plus the per-row
-//     rescale factors and running max/sum into the peer's shared memory with a
-//     bulk copy.
-//   rank 1, the output CTA: gathers V tiles [64 entries, 512], accumulates
-//     O += P V in TMEM, rescales O when the score CTA raised its reference max,
-//     and writes O / l and the log-sum-exp (or the split partial and the fused
-//     split merge).
+//   ranks 0 and 1, the score pair: rank h holds query rows [128h, 128h+128) of
+//     the item in TMEM (the A operand).  Each 128-entry KV tile is gathered
+//     once per pair: rank h gathers entries [64h, 64h+64) of the tile, all 576
+//     columns.  One cta_group::2 MMA per 16 columns (M = 256 rows, N = 128
+//     entries, each CTA supplying half of N) writes S = Q K^T of the CTA's own
+//     rows into its TMEM, so every gathered byte serves 256 query rows.  Eight
+//     row warps per CTA run the masked online softmax (two threads per query
+//     row, 64 entries each, exchanging the row max through shared memory) and
+//     ship P (bf16) with the per-row rescale factor and running max/sums to the
+//     output CTA of the same half with one bulk copy.
+//   ranks 2 and 3, the output pair: O[256, 512] accumulates in fp32 TMEM, rank
+//     2+h holding the rows of half h.  PV runs as cta_group::2 MMAs of M = 256,
+//     N = 256: for latent columns [256c, 256c+256) rank 2 supplies V columns
+//     [256c, 256c+128) and rank 3 [256c+128, 256c+256), so each output CTA
+//     gathers half of the 512 latent columns of every entry.  Their row warps
+//     (two per row, 256 columns each) rescale O when the score side raised its
+//     reference max and write O / l and the log-sum-exp (or the split partial
+//     and the fused split merge).
 //
-// The KV tile in shared memory is stored as 64-column chunks in the 128-byte
-// swizzled layout, so the same bytes serve as the K-major B operand of QK^T and
-// as the MN-major B operand of PV.  fp8 e4m3 pools are gathered as bytes and
-// converted to bf16 in registers by dedicated warps (exact: e4m3 -> f16 by the
-// hardware conversion, then the f16 bits are placed in a bf16 word, which
-// scales every value by 2^-112; the factor is folded into the logit and output
-// scales).
+// KV tiles sit in shared memory as 64-column chunks in the 128-byte swizzled
+// layout: the score CTAs read them as the K-major B operand of QK^T, the output
+// CTAs as the MN-major B operand of PV.  A TMA gather op costs its issuing warp
+// about a hundred cycles, so seven warps share a tile's ops.  fp8 e4m3 pools
+// are gathered as bytes and converted to bf16 in registers by four warps
+// (exact: e4m3 -> f16 by the hardware conversion, then the f16 bits are placed
+// in a bf16 word, which scales every value by 2^-112; the factor is folded into
+// the logit and output scales).  The MMA of a pair is issued by its even rank;
+// the odd rank relays "my half of the tile is in place" to it through a
+// cluster mbarrier.
 //
 // Sources: absorbed-latent MLA decode with one 576-wide latent row per KV entry
 // ("[ROCm] Dspark MLA module", Details); page-size-1 index lists and the
@@ -42,64 +53,90 @@ namespace {
 
 using namespace tc;
 
-// 12 warps for bf16 pools (seven of them gather), 10 for fp8 (warps 10-11 would
-// only slow the conversion warps down).
-constexpr int threads_for(bool fp8) { return fp8 ? 320 : 384; }
-constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpRow0 = 2;           // 4 row warps: softmax (rank 0) / correction+epilogue (rank 1)
-constexpr int kWarpConv0 = 6;          // 4 fp8 conversion warps (bf16: KV gathers)
+// 16 warps, 128 registers each:
+//   0-7   row warps: TMEM lane quadrant warp & 3, column half warp >> 2
+//   8     MMA issue (even rank) / relay (odd rank); owns TMEM
+//   9-15  bf16: TMA gathers; fp8: 9, 14, 15 gather the raw rows, 10-13 convert
+constexpr int kThreads = 512;
+constexpr int kRowWarps = 8;
+constexpr int kWarpMma = 8;
+constexpr int kWarpAux0 = 9;
+constexpr int kConvWarps = 4;
+constexpr int kWarpConv0 = 10;
 constexpr int kStages = 2;             // KV tile ring
 constexpr int kPBufs = 2;              // P hand-off ring
 
-constexpr int kChunkBytes = kBlockN * 128;          // 64 entries x 64 bf16 columns = 8 KB
-constexpr int kKTileBytes = 9 * kChunkBytes;        // 576 columns (score CTA)
-// fp8: the tile's raw e4m3 rows are gathered into the upper half of the stage
-// (three 192-byte column blocks of [64 rows][192 B]) and converted in place.
-constexpr int kF8Off = kKTileBytes / 2;             // 36 KB
-constexpr int kF8BlockBytes = kBlockN * 192;        // 12 KB
-constexpr int kPBytes = kRows * 128;                // P: 128 rows x 64 bf16
-constexpr int kPStatsOff = kPBytes;                 // alpha[128], m[128], l[128], flags[4]
-constexpr int kPBufBytes = kPBytes + 3 * 512 + 512; // 18 KB, multiple of 16
+constexpr int kTileN = kBlockN;        // 128 entries per tile
+constexpr int kHalfN = kTileN / 2;     // entries gathered by one score CTA
+constexpr int kHalfRows = kRows / 2;   // 128 query rows per CTA
+static_assert(kTileN == 128 && kHalfRows == 128, "tile geometry");
 
-// Shared-memory map (identical offsets in both CTAs; barriers first).
+constexpr int kSChunk = kHalfN * 128;          // score: [64 entries][64 bf16 columns] = 8 KB
+constexpr int kStageBytes = 9 * kSChunk;       // score stage: 576 columns, 72 KB
+constexpr int kOChunk = kTileN * 128;          // output: [128 entries][64 columns] = 16 KB
+constexpr int kOStageUsed = 4 * kOChunk;       // output stage: 4 column chunks, 64 KB
+// fp8 raw rows land in the upper part of a stage and are converted in place.
+constexpr int kF8SOff = kStageBytes / 2;       // score: 64 rows x 576 B at 36 KB
+constexpr int kF8SBlock = kHalfN * 192;        //   three [64][192 B] column blocks
+constexpr int kF8OOff = kOStageUsed / 2;       // output: 128 rows x 2 x 128 B at 32 KB
+constexpr int kF8OBlock = kTileN * 128;        //   two [128][128 B] column blocks
+constexpr int kPChunk = kHalfRows * 128;       // P: [128 rows][64 entries bf16] = 16 KB
+constexpr int kPBytes = 2 * kPChunk;           // 128 entries
+constexpr int kPStatsOff = kPBytes;            // alpha[128], m[128], l[2][128] (per column half), flags[4]
+constexpr int kPCopyBytes = kPBytes + 4 * 512 + 64;  // bytes handed over per tile, a multiple of 16
+constexpr int kPBufBytes = 35 * 1024;          // buffer stride: each P buffer starts on a swizzle atom
+
+// Shared-memory map (identical offsets in all four CTAs; barriers first).
 constexpr int kOffBars = 0;
-constexpr int kOffData = 2048;
-constexpr int kOffTiles = kOffData;                                   // kStages x 72 KB
-constexpr int kOffPBuf = kOffTiles + kStages * kKTileBytes;           // kPBufs x 18 KB
-constexpr int kOffEpi = kOffPBuf + kPBufs * kPBufBytes;              // output CTA: 4 x 4 KB epilogue staging
-constexpr int kSmemBytes = kOffEpi + 4 * 4096;
+constexpr int kOffRed = 1024;                                     // score: row-max exchange [2][2][128] fp32
+constexpr int kOffTiles = 3072;                                   // kStages x 72 KB
+constexpr int kOffPBuf = kOffTiles + kStages * kStageBytes;       // kPBufs P buffers
+constexpr int kSmemBytes = kOffPBuf + kPBufs * kPBufBytes;
 constexpr int kSmemAlign = 1024;
+// Output CTAs: epilogue staging (8 warps x 2 KB) and merge weights live in the
+// last 8 KB of each stage, which their 64 KB of V never touches.
+constexpr int kOffEpi0 = kOffTiles + kOStageUsed;
+constexpr int kOffEpi1 = kOffTiles + kStageBytes + kOStageUsed;
+static_assert(kStageBytes - kOStageUsed == 8192, "epilogue staging");
+static_assert(kSmemBytes + kSmemAlign <= 232448, "shared memory");
+// Every operand the MMA reads through a 128-byte-swizzle descriptor starts on a
+// 1024-byte boundary (the swizzle is a function of the address bits).
+static_assert(kOffTiles % 1024 == 0 && kStageBytes % 1024 == 0 && kOffPBuf % 1024 == 0 &&
+                  kPBufBytes % 1024 == 0 && kPChunk % 1024 == 0 && kPCopyBytes % 16 == 0 &&
+                  kPCopyBytes <= kPBufBytes,
+              "alignment");
 
 // TMEM columns.
-constexpr uint32_t kTmemQ = 0;       // score CTA: Q as A operand, 288 columns
-constexpr uint32_t kTmemS = 288;     // score CTA: two 64-column S buffers
-constexpr uint32_t kTmemO = 0;       // output CTA: O, 512 columns
+constexpr uint32_t kTmemQ = 0;         // score: Q as A operand, 288 columns
+constexpr uint32_t kTmemS = 288;       // score: S, 128 columns
+constexpr uint32_t kTmemO = 0;         // output: O, 512 columns
 
 struct Bars {
-  uint64_t full[kStages];     // KV tile landed (TMA or fp8 conversion)
-  uint64_t empty[kStages];    // KV tile consumed by this CTA's MMA
-  uint64_t full8[kStages];    // fp8: raw e4m3 rows of the tile landed (TMA)
+  uint64_t full[kStages];     // this CTA's share of the tile is in place (TMA, or fp8 conversion)
+  uint64_t peer[kStages];     // even rank: the odd rank's share is in place (relayed)
+  uint64_t empty[kStages];    // the pair's MMA on this stage is done
+  uint64_t full8[kStages];    // fp8: raw e4m3 rows landed (TMA)
   uint64_t cv_sync;           // fp8: the conversion warps finished reading the raw rows
-  uint64_t s_full[2];         // score CTA: S tile computed
-  uint64_t s_free[2];         // score CTA: S tile read out
-  uint64_t q_full;            // score CTA: Q written to TMEM
-  uint64_t q_free;            // score CTA: all QK of the item done
-  uint64_t p_empty[kPBufs];   // score CTA: peer finished PV with P buffer
-  uint64_t p_ready[kPBufs];   // score CTA: the four softmax warps staged P
-  uint64_t p_full[kPBufs];    // output CTA: P buffer arrived
-  uint64_t corr_done[kPBufs]; // output CTA: O ready for PV on this P buffer
-  uint64_t o_ready[kPBufs];   // output CTA: PV with this P buffer complete
-  uint64_t o_free;            // output CTA: epilogue read O
-  uint64_t mrg_a;             // output CTA: the 4 row warps fenced their partial rows
-  uint64_t mrg_b;             // output CTA: leader published the last-arriver verdict
-  uint64_t mrg_c;             // output CTA: per-row merge weights ready
-  uint64_t mrg_d;             // output CTA: the 4 row warps are done with the weights
+  uint64_t q_full;            // score, even rank: Q of both CTAs written to TMEM
+  uint64_t q_free;            // score: every QK^T of the item done
+  uint64_t s_full;            // score: S computed
+  uint64_t s_free;            // score, even rank: S read out by both CTAs
+  uint64_t p_free[kPBufs];    // score: the PV that used this P buffer is done
+  uint64_t p_ready[kPBufs];   // score: the eight softmax warps staged P
+  uint64_t p_full[kPBufs];    // output: P buffer arrived
+  uint64_t corr[kPBufs];      // output, even rank: both CTAs hold P and have rescaled O
+  uint64_t o_ready[kPBufs];   // output: PV with this P buffer done
+  uint64_t o_free;            // output, even rank: both epilogues read O
+  uint64_t mrg_a;             // output: the row warps fenced their partial rows
+  uint64_t mrg_b;             // output: leader published the last-arriver verdict
+  uint64_t mrg_c;             // output: per-row merge weights ready
+  uint64_t mrg_d;             // output: the row warps are done with the weights
+  uint64_t never;             // failure-path test: nothing ever arrives here
   uint32_t tmem_base;
   int abort;
   int merge_last;
 };
-static_assert(sizeof(Bars) <= kOffData, "barrier block too large");
+static_assert(sizeof(Bars) <= kOffRed, "barrier block too large");
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -109,47 +146,71 @@ __device__ __forceinline__ float ex2(float x) {
 
 // 128-byte swizzle: byte offset of 16-byte unit u of row r inside a chunk.
 __device__ __forceinline__ uint32_t swz(int r, int u) { return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4)); }
+// Epilogue staging, 64-byte rows: unit u of row r (bank-conflict free for 8 rows).
+__device__ __forceinline__ uint32_t swz64(int r, int u) { return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4)); }
 
-// On a failed wait: record, raise the abort flag here and in the peer.
+// On a failed wait: record, raise the abort flag in all four CTAs.
 __device__ __noinline__ void fail(Bars* bars, const DecodeParams& p, int site) {
   record_error(p.ws_hdr, MLA_DEV_WAIT_TIMEOUT, site);
   bars->abort = 1;
-  const uint32_t peer = cluster_rank() ^ 1u;
-  const uint32_t a = mapa(smem_u32(&bars->abort), peer);
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+  for (uint32_t r = 0; r < 4; ++r) {
+    const uint32_t a = mapa(smem_u32(&bars->abort), r);
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+  }
 }
 
 // Warp-collective bounded waits: every lane polls, and the warp leaves together
-// (to the teardown) if any lane gave up.
-#define WAIT(bar, par, site)                                                         \
-  if (!__all_sync(0xffffffffu, mbar_wait(bar, par, &bars->abort))) {               \
-    fail(bars, p, site);                                                             \
-    goto done;                                                                       \
+// (to the teardown) if any lane gave up.  WAITC: barrier signalled from another CTA.
+#define WAIT(bar, par, site)                                                          \
+  if (!__all_sync(0xffffffffu, mbar_wait(bar, par, &bars->abort, p.wait_limit))) {   \
+    fail(bars, p, site);                                                              \
+    goto done;                                                                        \
   }
-#define WAITC(bar, par, site)                                                        \
-  if (!__all_sync(0xffffffffu, mbar_wait<true>(bar, par, &bars->abort))) {         \
-    fail(bars, p, site);                                                             \
-    goto done;                                                                       \
+#define WAITC(bar, par, site)                                                         \
+  if (!__all_sync(0xffffffffu, mbar_wait<true>(bar, par, &bars->abort, p.wait_limit))) { \
+    fail(bars, p, site);                                                              \
+    goto done;                                                                        \
   }
 
-// Static work assignment, identical in every role of both CTAs of a cluster:
-// round r gives cluster c item r*C + c on even rounds and r*C + (C-1-c) on odd
-// rounds, so a cost-sorted item list is dealt out boustrophedon-fashion.
+// Arrive on `bar` in CTA `to` (this CTA or another of the cluster).  Every
+// cross-CTA signal here orders only tcgen05 work the caller fenced with
+// tcgen05.fence::before_thread_sync (TMEM reads and writes) or data whose landing
+// the caller observed on its own barrier, so the remote arrive is relaxed.
+__device__ __forceinline__ void arrive_at(uint64_t* bar, uint32_t to, uint32_t self) {
+  if (to == self) mbar_arrive(bar);
+  else mbar_arrive_remote_relaxed(bar, to);
+}
+
+// Static work assignment, identical in every role of all four CTAs: round r
+// gives cluster c item r*C + c on even rounds and r*C + (C-1-c) on odd rounds,
+// so a cost-sorted item list is dealt out boustrophedon-fashion.
 __device__ __forceinline__ int item_of(int r, int c, int C) { return r * C + ((r & 1) ? C - 1 - c : c); }
 #define FOR_ITEMS(idx)                                                      \
   for (int r_ = 0, idx = item_of(0, cluster, n_clusters); idx < n_items; \
        ++r_, idx = item_of(r_, cluster, n_clusters))
 
-// Number of 64-entry tiles of an item.
+// Number of 128-entry tiles of an item (the same in all four CTAs).
 __device__ __forceinline__ int item_tiles(const Item& it) {
-  return it.ok && it.e1 > it.e0 ? (it.e1 - it.e0 + kBlockN - 1) / kBlockN : 0;
+  return it.ok && it.e1 > it.e0 ? (it.e1 - it.e0 + kTileN - 1) / kTileN : 0;
 }
 
-// 16 e4m3 values (unit u of 64-column chunk c of tile row `row`) -> two 16-byte
-// bf16 units of the swizzled tile.  Exact: the f16 bits from the hardware e4m3
-// conversion are placed in a bf16 word with the same exponent field, which
-// scales every value by 2^-112 (folded into the logit and output scales).
-__device__ __forceinline__ void fp8_unit_to_tile(uint8_t* stage, int row, int c, int u, const uint4& v) {
+// Pull one half's query rows of item `idx` into L2 ahead of their TMEM load.
+__device__ __forceinline__ void prefetch_q_rows(const DecodeParams& p, int idx, int n_items, int half) {
+  if (idx >= n_items) return;
+  const Item it = load_item(p, idx);
+  if (!it.ok) return;
+  const int hrows = min(max(it.nrows - kHalfRows * half, 0), kHalfRows);
+  if (hrows <= 0) return;
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(static_cast<const uint16_t*>(p.q) +
+                                                        (it.q_row_base + it.row0 + kHalfRows * half) * kDqk);
+  const uint32_t bytes = (uint32_t)hrows * kDqk * 2;
+  for (uint32_t o = 0; o < bytes; o += 16384) prefetch_l2_bulk(src + o, bytes - o < 16384 ? bytes - o : 16384);
+}
+
+// 16 e4m3 values -> two 16-byte bf16 units at dst0 / dst1.  Exact: the f16 bits
+// from the hardware e4m3 conversion are placed in a bf16 word with the same
+// exponent field, which scales every value by 2^-112 (folded into the scales).
+__device__ __forceinline__ void fp8_unit_to_bf16(uint8_t* dst0, uint8_t* dst1, const uint4& v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   uint32_t o[8];
 #pragma unroll
@@ -160,187 +221,217 @@ __device__ __forceinline__ void fp8_unit_to_tile(uint8_t* stage, int row, int c,
     o[2 * q] = ((h0 & 0x7FFF7FFFu) >> 3) | (h0 & 0x80008000u);
     o[2 * q + 1] = ((h1 & 0x7FFF7FFFu) >> 3) | (h1 & 0x80008000u);
   }
-  uint8_t* base = stage + c * kChunkBytes;
-  *reinterpret_cast<uint4*>(base + swz(row, 2 * u)) = make_uint4(o[0], o[1], o[2], o[3]);
-  *reinterpret_cast<uint4*>(base + swz(row, 2 * u + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
+  *reinterpret_cast<uint4*>(dst0) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(dst1) = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
-// Epilogue write-back of one 32-column block of a warp's 32 rows, staged at stg
-// (128-byte row pitch, 16-byte unit k of row r at unit k ^ (r & 7)): each store
-// instruction writes whole row segments, 128 bytes (fp32) or 64 bytes (bf16).
-template <bool kF32>
-__device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q4, int c, const Item& it,
-                                             const DecodeParams& p) {
-  constexpr int kUsh = kF32 ? 3 : 2;          // log2 of 16-byte units per row segment
-  constexpr int kN = 1 << kUsh;
-  uint4 val[kN];
+// Epilogue write-back of a 64-byte column segment (32 bf16 or 16 fp32 columns
+// starting at column `col`) of a warp's 32 rows, staged at stg as [32][64 B]:
+// each store instruction writes eight whole 64-byte row segments.
+__device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q4, int col, bool f32,
+                                             const Item& it, int half, int hrows, const DecodeParams& p) {
+  uint4 val[4];
 #pragma unroll
-  for (int i = 0; i < kN; ++i) {
-    const int rl = (i << (5 - kUsh)) + (lane >> kUsh), u = lane & (kN - 1);
-    val[i] = *reinterpret_cast<const uint4*>(stg + rl * 128 + ((u ^ (rl & 7)) << 4));
+  for (int i = 0; i < 4; ++i) {
+    const int rl = 8 * i + (lane >> 2), u = lane & 3;
+    val[i] = *reinterpret_cast<const uint4*>(stg + swz64(rl, u));
   }
 #pragma unroll
-  for (int i = 0; i < kN; ++i) {
-    const int rl = (i << (5 - kUsh)) + (lane >> kUsh), u = lane & (kN - 1);
-    const int ri = 32 * q4 + rl;               // row within the item
-    if (ri < it.nrows) {
+  for (int i = 0; i < 4; ++i) {
+    const int rl = 8 * i + (lane >> 2), u = lane & 3;
+    const int ri = 32 * q4 + rl;                 // row within this half
+    if (ri < hrows) {
+      const int64_t irow = kHalfRows * half + ri;   // row within the item
       void* dst;
-      if (!kF32) dst = static_cast<__nv_bfloat16*>(p.o) + (it.q_row_base + it.row0 + ri) * kDv + 32 * c + 8 * u;
-      else if (it.slot >= 0) dst = p.part_o + ((int64_t)it.slot * kRows + ri) * kDv + 32 * c + 4 * u;
-      else dst = static_cast<float*>(p.o) + (it.q_row_base + it.row0 + ri) * kDv + 32 * c + 4 * u;
+      if (!f32) dst = static_cast<__nv_bfloat16*>(p.o) + (it.q_row_base + it.row0 + irow) * kDv + col + 8 * u;
+      else if (it.slot >= 0) dst = p.part_o + ((int64_t)it.slot * kRows + irow) * kDv + col + 4 * u;
+      else dst = static_cast<float*>(p.o) + (it.q_row_base + it.row0 + irow) * kDv + col + 4 * u;
       *reinterpret_cast<uint4*>(dst) = val[i];
     }
   }
 }
 
 template <bool kFp8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_for(kFp8), 1)
-mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const DecodeParams p) {
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
+mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                         const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t rank = cluster_rank();
-  const bool score_cta = rank == 0;
+  const int half = (int)(rank & 1u);              // row half of the item / B half of the pair
+  const bool score_cta = rank < 2;
+  const bool even = half == 0;                    // issues the pair's MMAs
+  const uint32_t lead = rank & ~1u;               // even rank of this CTA's pair
+  const uint32_t out_peer = rank ^ 2u;            // same half on the other side
 
   if (!plan_header_ok(p.plan, p)) {
     if (blockIdx.x == 0 && tid == 0) record_error(p.ws_hdr, MLA_DEV_PLAN_MISMATCH, 0);
-    return;   // both CTAs of every cluster leave before touching each other
+    return;   // every CTA of every cluster leaves before touching another
   }
   const int n_items = p.plan[kHNItems];
   const int cluster = (int)cluster_id_x(), n_clusters = (int)num_clusters_x();
+  if (score_cta && tid == 0) prefetch_q_rows(p, item_of(0, cluster, n_clusters), n_items, half);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bars->full[s], kFp8 ? 4 : 1);
+      mbar_init(&bars->full[s], kFp8 ? kConvWarps : 1);
+      mbar_init(&bars->peer[s], 1);
       mbar_init(&bars->empty[s], 1);
       mbar_init(&bars->full8[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bars->s_full[b], 1);
-      mbar_init(&bars->s_free[b], 4);
-    }
-    mbar_init(&bars->q_full, 4);
+    mbar_init(&bars->cv_sync, kConvWarps);
+    mbar_init(&bars->q_full, 2 * kRowWarps);
     mbar_init(&bars->q_free, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 2 * kRowWarps);
     for (int b = 0; b < kPBufs; ++b) {
-      mbar_init(&bars->p_empty[b], 1);
-      mbar_init(&bars->p_ready[b], 4);
+      mbar_init(&bars->p_free[b], 1);
+      mbar_init(&bars->p_ready[b], kRowWarps);
       mbar_init(&bars->p_full[b], 1);
-      mbar_init(&bars->corr_done[b], 4);
+      mbar_init(&bars->corr[b], 2 * kRowWarps);
       mbar_init(&bars->o_ready[b], 1);
     }
-    mbar_init(&bars->o_free, 4);
-    mbar_init(&bars->cv_sync, 4);
-    mbar_init(&bars->mrg_a, 4);
+    mbar_init(&bars->o_free, 2 * kRowWarps);
+    mbar_init(&bars->mrg_a, kRowWarps);
     mbar_init(&bars->mrg_b, 1);
-    mbar_init(&bars->mrg_c, 4);
-    mbar_init(&bars->mrg_d, 4);
+    mbar_init(&bars->mrg_c, kRowWarps);
+    mbar_init(&bars->mrg_d, kRowWarps);
+    mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
-    tmem_alloc(&bars->tmem_base, 512);
-    tmem_relinquish();
+    tmem_alloc2(&bars->tmem_base, 512);
+    tmem_relinquish2();
   }
-  if (warp == kWarpProducer && lane == 0) prefetch_tmap(&tmap_kv);
+  if (warp == kWarpAux0 && lane == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
   fence_before_sync();
   __syncthreads();
-  cluster_sync();        // barriers of both CTAs initialised before any remote arrival
+  cluster_sync();        // barriers of all four CTAs initialised before any remote arrival
   fence_after_sync();
   const uint32_t tmem = bars->tmem_base;
   uint8_t* tiles = smem + kOffTiles;
   uint8_t* pbufs = smem + kOffPBuf;
+  // Failure-path test: every warp waits on a barrier nothing signals, before any
+  // copy or MMA is issued, so the bounded wait runs out with nothing in flight
+  // and the kernel records the timeout and tears down.
+  if (p.test_stall) {
+    WAIT(&bars->never, 0, 99);
+  }
 
-  // ======================================================================= producer
-  // KV gathers with TMA.  One gather op moves 4 rows (entries 4g..4g+3, row
-  // group g) x one column block; a tile needs 16 groups x nblk blocks.  Issue
-  // cost is mostly per warp instruction, so each lane owns one op and a warp
-  // issues its share of the tile in one instruction (two for fp8).
-  //   bf16: each CTA gathers the 64-column chunks it reads into its own ring
-  //   (score CTA: all 9, output CTA: the 8 latent chunks), so the score CTA
-  //   refills a stage as soon as its QK^T is done with it; warps 0 and 6-11 share
-  //   the 144 (128) ops.
-  //   fp8: the raw e4m3 rows, three 192-byte column blocks per row, land in the
-  //   stage's upper half for the conversion warps; warp 0 issues the 48 ops
-  //   alone (more issuing warps slowed the conversion warps beside them).
-  if (warp == kWarpProducer || (!kFp8 && warp >= kWarpConv0)) {
-    constexpr int npw = kFp8 ? 1 : 7;
-    constexpr int kOpsPerLane = kFp8 ? 2 : 1;
-    const int pw = warp == kWarpProducer ? 0 : warp - kWarpConv0 + 1;
-    const int nblk = kFp8 ? 3 : (score_cta ? 9 : 8);
-    const int nops = 16 * nblk;
-    const int per = (nops + npw - 1) / npw;             // ops of this warp: [o_begin, o_end)
+  // ======================================================================= producers
+  // KV gathers with TMA.  One gather op moves 4 rows (entries 4g..4g+3) x one
+  // column box; each lane of an issuing warp owns at most one op of the tile.
+  //   score CTA h: entries [64h, 64h+64) of the tile, 9 column chunks (bf16: 144
+  //     ops; fp8: three 192-byte boxes per row, 48 ops, into the stage's upper half);
+  //   output CTA h: all 128 entries, latent columns [128h, 128h+128) and
+  //     [256+128h, 256+128h+128) (bf16: 4 chunks, 128 ops; fp8: two 128-byte
+  //     boxes per row, 64 ops, into the upper half of its 64 KB).
+  if (warp >= kWarpAux0 && (!kFp8 || warp < kWarpConv0 || warp >= kWarpConv0 + kConvWarps)) {
+    constexpr int npw = kFp8 ? 3 : 7;                        // issuing warps
+    const int pw = (!kFp8 || warp == kWarpAux0) ? warp - kWarpAux0 : warp - (kWarpConv0 + kConvWarps) + 1;
+    const int ngroups = score_cta ? kHalfN / 4 : kTileN / 4;  // 16 | 32 groups of 4 entries
+    const int nblk = kFp8 ? (score_cta ? 3 : 2) : (score_cta ? 9 : 4);
+    const int nops = ngroups * nblk;
+    const int per = (nops + npw - 1) / npw;                   // ops of this warp: [o_begin, o_end), <= 32
     const int o_begin = pw * per, o_end = o_begin + per < nops ? o_begin + per : nops;
-    const uint32_t tx = (uint32_t)(16 * nblk * (kFp8 ? 4 * 192 : 512));
+    const uint32_t tx = (uint32_t)(score_cta ? (kFp8 ? kHalfN * 576 : kStageBytes)
+                                              : (kFp8 ? kTileN * 256 : kOStageUsed));
+    const int e_sub = score_cta ? kHalfN * half : 0;          // first tile entry this CTA gathers
+    const int nidx = ngroups / 8;                             // index registers in use (2 | 4)
+    const void* tmap = score_cta ? (const void*)&tmap_k : (const void*)&tmap_v;
     uint32_t kseq = 0;
-    const bool report = score_cta && pw == 0;
-    // Raw slot indices of tile j (lane holds entries lane and lane+32), -1 past the
-    // end; checked only when used, one iteration later, so the load is not waited on.
-    auto tile_idx = [&](const Item& it, int j, int32_t& x0, int32_t& x1) {
-      const int i0 = it.e0 + j * kBlockN + lane, i1 = i0 + 32;
-      x0 = i0 < it.e1 ? __ldg(p.kv_indices + it.kv_off + i0) : -1;
-      x1 = i1 < it.e1 ? __ldg(p.kv_indices + it.kv_off + i1) : -1;
+    const bool report = pw == 0;
+    // Raw slot indices of tile j: lane holds entries lane + 32k (k < nidx), -1 past
+    // the end; checked only when used, one iteration later, so the load is not waited on.
+    auto tile_idx = [&](const Item& it, int j, int32_t (&x)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = it.e0 + j * kTileN + e_sub + lane + 32 * k;
+        x[k] = (k < nidx && i < it.e1) ? __ldg(p.kv_indices + it.kv_off + i) : -1;
+      }
     };
     // Invalid entries read row -1 (zero fill) and are reported once.
-    auto checked = [&](const Item& it, int j, int half, int32_t v) -> int32_t {
+    auto checked = [&](const Item& it, int j, int k, int32_t v) -> int32_t {
       if (v >= 0 && v < p.num_slots) return v;
-      const int i = it.e0 + j * kBlockN + lane + 32 * half;
-      if (report && i < it.e1) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
+      const int i = it.e0 + j * kTileN + e_sub + lane + 32 * k;
+      if (report && k < nidx && i < it.e1) record_error(p.ws_hdr, MLA_DEV_BAD_INDEX, (int)(it.kv_off + i));
       return -1;
     };
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
-      int32_t n0 = -1, n1 = -1;
-      if (nt > 0) tile_idx(it, 0, n0, n1);
+      int32_t nx[4] = {-1, -1, -1, -1};
+      if (nt > 0) tile_idx(it, 0, nx);
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         const uint32_t ph = (kseq / kStages) & 1;
-        // this tile's indices were loaded one iteration ago; start the next tile's now
-        const int32_t r0 = checked(it, j, 0, n0), r1 = checked(it, j, 1, n1);
-        if (j + 1 < nt) tile_idx(it, j + 1, n0, n1);
-        // slot indices of the group of each of this lane's ops, from lanes
-        // (4g..4g+3) % 32 of r0 (g < 8) or r1 (g >= 8), before the wait
-        int32_t a[kOpsPerLane][4];
+        int32_t cx[4];
 #pragma unroll
-        for (int q = 0; q < kOpsPerLane; ++q) {
-          const int g = ((o_begin + 32 * q + lane) / nblk) & 15;
+        for (int k = 0; k < 4; ++k) cx[k] = checked(it, j, k, nx[k]);
+        if (j + 1 < nt) tile_idx(it, j + 1, nx);
+        // slot indices of this lane's op: group g's entries 4g..4g+3 sit in lanes
+        // (4g..4g+3) % 32 of index register g / 8
+        const int o = o_begin + lane;
+        const int g = (o < o_end ? o : o_begin) / nblk;
+        int32_t a[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int32_t x0 = __shfl_sync(0xffffffffu, r0, ((4 * g) & 31) + e);
-            const int32_t x1 = __shfl_sync(0xffffffffu, r1, ((4 * g) & 31) + e);
-            a[q][e] = g < 8 ? x0 : x1;
-          }
+        for (int e = 0; e < 4; ++e) {
+          const int src = ((4 * g) & 31) + e;
+          const int32_t v0 = __shfl_sync(0xffffffffu, cx[0], src);
+          const int32_t v1 = __shfl_sync(0xffffffffu, cx[1], src);
+          const int32_t v2 = __shfl_sync(0xffffffffu, cx[2], src);
+          const int32_t v3 = __shfl_sync(0xffffffffu, cx[3], src);
+          const int k = g >> 3;
+          a[e] = k == 0 ? v0 : k == 1 ? v1 : k == 2 ? v2 : v3;
         }
-        WAIT(&bars->empty[st], ph ^ 1, 1);
+        WAITC(&bars->empty[st], ph ^ 1, 1);
         uint64_t* bar = kFp8 ? &bars->full8[st] : &bars->full[st];
         if (pw == 0 && lane == 0) mbar_arrive_expect_tx(bar, tx);
         __syncwarp();
-        const uint32_t base = smem_u32(tiles + st * kKTileBytes);
-#pragma unroll
-        for (int q = 0; q < kOpsPerLane; ++q) {
-          const int o = o_begin + 32 * q + lane;
-          if (o < o_end) {
-            const int g = o / nblk, c = o - g * nblk;
-            if (kFp8)
-              tma_gather4(base + (uint32_t)(kF8Off + c * kF8BlockBytes + g * 4 * 192), &tmap_kv, 192 * c, a[q][0],
-                          a[q][1], a[q][2], a[q][3], bar);
-            else
-              tma_gather4(base + (uint32_t)(c * kChunkBytes + g * 512), &tmap_kv, c * 64, a[q][0], a[q][1], a[q][2],
-                          a[q][3], bar);
+        const uint32_t base = smem_u32(tiles + st * kStageBytes);
+        if (o < o_end) {
+          const int c = o - g * nblk;
+          uint32_t dst;
+          int32_t col;
+          if (kFp8) {
+            if (score_cta) {
+              dst = base + (uint32_t)(kF8SOff + c * kF8SBlock + g * 4 * 192);
+              col = 192 * c;
+            } else {
+              dst = base + (uint32_t)(kF8OOff + c * kF8OBlock + g * 4 * 128);
+              col = 256 * c + 128 * half;
+            }
+          } else if (score_cta) {
+            dst = base + (uint32_t)(c * kSChunk + g * 512);
+            col = 64 * c;
+          } else {
+            dst = base + (uint32_t)(c * kOChunk + g * 512);
+            col = 64 * (c < 2 ? 2 * half + c : 4 + 2 * half + (c - 2));
           }
+          tma_gather4(dst, tmap, col, a[0], a[1], a[2], a[3], bar);
         }
         __syncwarp();
       }
     }
+    // Drain: the pair's last MMA commits on `empty` must land before this CTA exits.
+    if (pw == 0)
+      for (int k = 0; k < kStages && (int)kseq - 1 - k >= 0; ++k) {
+        const uint32_t s = kseq - 1 - k;
+        WAITC(&bars->empty[s % kStages], (s / kStages) & 1, 2);
+      }
   }
   // ======================================================================= fp8: convert in place
-  // The four conversion warps turn the tile's raw e4m3 rows (gathered by warp 0
-  // into the stage's upper half) into the swizzled bf16 tile.  Warp cw owns rows
-  // 16cw .. 16cw+15.  Chunks 0-3 are written first (below the raw rows); the raw
-  // bytes of chunks 4.. are read into registers, and once all four warps hold
-  // theirs the remaining chunks overwrite the raw area.
-  else if (kFp8 && warp >= kWarpConv0) {
+  // The conversion warps turn the stage's raw e4m3 rows into the swizzled bf16
+  // tile.  Rows are split between the warps.  The chunks that land below the raw
+  // area are written first; the raw bytes of the rest go to registers, and once
+  // every conversion warp holds its share the remaining chunks overwrite the raw area.
+  else if (kFp8 && warp >= kWarpConv0 && warp < kWarpConv0 + kConvWarps) {
     const int cw = warp - kWarpConv0;
     uint32_t kseq = 0, cv_ph = 0;
     FOR_ITEMS(idx) {
@@ -349,34 +440,66 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         WAIT(&bars->full8[st], (kseq / kStages) & 1, 4);
-        uint8_t* stage = tiles + st * kKTileBytes;
-        const uint8_t* raw = stage + kF8Off;
-        // chunks 0-3: 16 rows x 4 chunks x 4 units of 16 fp8 values, 8 per lane
+        uint8_t* stage = tiles + st * kStageBytes;
+        if (score_cta) {
+          // 64 rows x 36 units of 16 e4m3 values; warp cw owns rows kR*cw ...
+          // Chunk c, unit u (of 4 per 64 columns) is raw unit 4c+u of the row, in
+          // column block (4c+u)/12 at offset ((4c+u)%12)*16.
+          constexpr int kR = kHalfN / kConvWarps;     // 16 rows per warp
+          const uint8_t* raw = stage + kF8SOff;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int f = k * 32 + lane, row = 16 * cw + (f >> 4), c = (f >> 2) & 3, u = f & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(raw + (c / 3) * kF8BlockBytes + row * 192 + (c % 3) * 64 + u * 16);
-          fp8_unit_to_tile(stage, row, c, u, v);
-        }
-        // chunks 4.. (score: 4-8, output: 4-7) into registers
-        uint4 rb[10];
-        const int nb = score_cta ? 5 : 4;
-#pragma unroll
-        for (int k = 0; k < 10; ++k) {
-          if (k < 2 * nb) {
-            const int f = k * 32 + lane, row = 16 * cw + f / (4 * nb), c = 4 + (f % (4 * nb)) / 4, u = f & 3;
-            rb[k] = *reinterpret_cast<const uint4*>(raw + (c / 3) * kF8BlockBytes + row * 192 + (c % 3) * 64 + u * 16);
+          for (int k = 0; k < kR * 16 / 32; ++k) {    // chunks 0-3: kR rows x 16 units
+            const int f = k * 32 + lane, row = kR * cw + (f >> 4), c = (f >> 2) & 3, u = f & 3;
+            const int ru = 4 * c + u;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + (ru / 12) * kF8SBlock + row * 192 + (ru % 12) * 16);
+            uint8_t* ch = stage + c * kSChunk;
+            fp8_unit_to_bf16(ch + swz(row, 2 * u), ch + swz(row, 2 * u + 1), v);
           }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->cv_sync);
-        WAIT(&bars->cv_sync, cv_ph, 5);
-        cv_ph ^= 1;
+          uint4 rb[kR * 20 / 32];                     // chunks 4-8: kR rows x 20 units
 #pragma unroll
-        for (int k = 0; k < 10; ++k) {
-          if (k < 2 * nb) {
-            const int f = k * 32 + lane, row = 16 * cw + f / (4 * nb), c = 4 + (f % (4 * nb)) / 4, u = f & 3;
-            fp8_unit_to_tile(stage, row, c, u, rb[k]);
+          for (int k = 0; k < kR * 20 / 32; ++k) {
+            const int f = k * 32 + lane, row = kR * cw + f / 20, c = 4 + (f % 20) / 4, u = f & 3;
+            const int ru = 4 * c + u;
+            rb[k] = *reinterpret_cast<const uint4*>(raw + (ru / 12) * kF8SBlock + row * 192 + (ru % 12) * 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->cv_sync);
+          WAIT(&bars->cv_sync, cv_ph, 5);
+          cv_ph ^= 1;
+#pragma unroll
+          for (int k = 0; k < kR * 20 / 32; ++k) {
+            const int f = k * 32 + lane, row = kR * cw + f / 20, c = 4 + (f % 20) / 4, u = f & 3;
+            uint8_t* ch = stage + c * kSChunk;
+            fp8_unit_to_bf16(ch + swz(row, 2 * u), ch + swz(row, 2 * u + 1), rb[k]);
+          }
+        } else {
+          // 128 rows x 16 units; warp cw owns rows kR*cw ...  Raw unit ru of a row
+          // sits in column block ru/8 at offset (ru%8)*16 and becomes units
+          // 2(ru%4), 2(ru%4)+1 of chunk slot ru/4.
+          constexpr int kR = kTileN / kConvWarps;     // 32 rows per warp
+          const uint8_t* raw = stage + kF8OOff;
+#pragma unroll
+          for (int k = 0; k < kR * 8 / 32; ++k) {     // slots 0-1 (raw block 0): kR rows x 8 units
+            const int f = k * 32 + lane, row = kR * cw + (f >> 3), ru = f & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(raw + row * 128 + ru * 16);
+            uint8_t* ch = stage + (ru >> 2) * kOChunk;
+            fp8_unit_to_bf16(ch + swz(row, 2 * (ru & 3)), ch + swz(row, 2 * (ru & 3) + 1), v);
+          }
+          uint4 rb[kR * 8 / 32];                      // slots 2-3 (raw block 1)
+#pragma unroll
+          for (int k = 0; k < kR * 8 / 32; ++k) {
+            const int f = k * 32 + lane, row = kR * cw + (f >> 3), ru = f & 7;
+            rb[k] = *reinterpret_cast<const uint4*>(raw + kF8OBlock + row * 128 + ru * 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->cv_sync);
+          WAIT(&bars->cv_sync, cv_ph, 5);
+          cv_ph ^= 1;
+#pragma unroll
+          for (int k = 0; k < kR * 8 / 32; ++k) {
+            const int f = k * 32 + lane, row = kR * cw + (f >> 3), ru = f & 7;
+            uint8_t* ch = stage + (2 + (ru >> 2)) * kOChunk;
+            fp8_unit_to_bf16(ch + swz(row, 2 * (ru & 3)), ch + swz(row, 2 * (ru & 3) + 1), rb[k]);
           }
         }
         fence_proxy_async_smem();
@@ -385,125 +508,139 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       }
     }
   }
-  // ======================================================================= score CTA: MMA
+  // ======================================================================= odd ranks: relay
+  // Tell the even rank of the pair that this CTA's share of the tile is in place.
+  else if (!even && warp == kWarpMma) {
+    uint32_t kseq = 0;
+    FOR_ITEMS(idx) {
+      const Item it = load_item(p, idx);
+      const int nt = item_tiles(it);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages;
+        WAIT(&bars->full[st], (kseq / kStages) & 1, 6);
+        if (lane == 0) mbar_arrive_remote_relaxed(&bars->peer[st], lead);
+        __syncwarp();
+      }
+    }
+  }
+  // ======================================================================= score pair: MMA (rank 0)
   else if (score_cta && warp == kWarpMma) {
-    uint32_t kseq = 0, sseq = 0, qitem = 0;
-    const uint32_t idesc = idesc_bf16_f32(128, kBlockN, false, false);
+    uint32_t kseq = 0, qitem = 0;
+    const uint32_t idesc = idesc_bf16_f32(256, kTileN, false, false);
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
-      WAIT(&bars->q_full, qitem & 1, 10);
-      fence_after_sync();
-      for (int j = 0; j < nt; ++j, ++kseq, ++sseq) {
-        const int st = kseq % kStages, sb = sseq & 1;
-        WAIT(&bars->s_free[sb], ((sseq >> 1) & 1) ^ 1, 11);
+      WAITC(&bars->q_full, qitem & 1, 10);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages;
         const uint32_t kph = (kseq / kStages) & 1;
-        // B descriptor of K step k: chunk k/4, 32-byte column offset k%4 (start address field is addr>>4)
-        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), 16, 1024);
-        const uint32_t dS = tmem + kTmemS + sb * kBlockN;
-        WAITC(&bars->full[st], kph, 12);
+        WAITC(&bars->s_free, (kseq & 1) ^ 1, 11);
+        WAIT(&bars->full[st], kph, 12);
+        WAITC(&bars->peer[st], kph, 13);
         fence_after_sync();
         if (lane == 0) {
+          // B descriptor of K step k: chunk k/4, 32-byte column offset k%4
+          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kStageBytes), 16, 1024);
 #pragma unroll
           for (int k = 0; k < kDqk / 16; ++k)
-            mma_ts(dS, tmem + kTmemQ + 8 * k, bdesc0 + (uint64_t)(((k >> 2) * kChunkBytes + (k & 3) * 32) >> 4),
-                   idesc, k > 0);
-          mma_commit(&bars->empty[st]);
-          mma_commit(&bars->s_full[sb]);
+            mma2_ts(tmem + kTmemS, tmem + kTmemQ + 8 * k,
+                    bdesc0 + (uint64_t)(((k >> 2) * kSChunk + (k & 3) * 32) >> 4), idesc, k > 0);
+          mma2_commit_mc(&bars->empty[st], 0x3);
+          mma2_commit_mc(&bars->s_full, 0x3);
         }
         __syncwarp();
       }
-      if (lane == 0) mma_commit(&bars->q_free);
+      if (lane == 0) mma2_commit_mc(&bars->q_free, 0x3);
       __syncwarp();
       ++qitem;
     }
   }
-  // ======================================================================= output CTA: MMA
-  else if (!score_cta && warp == kWarpMma) {
-    uint32_t kseq = 0, pseq = 0, oitem = 0;
-    const uint32_t idesc = idesc_bf16_f32(128, 256, false, true);
+  // ======================================================================= output pair: MMA (rank 2)
+  else if (warp == kWarpMma) {
+    uint32_t kseq = 0, oitem = 0;
+    const uint32_t idesc = idesc_bf16_f32(256, 256, false, true);
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
-      WAIT(&bars->o_free, (oitem & 1) ^ 1, 20);
-      for (int j = 0; j < nt; ++j, ++kseq, ++pseq) {
-        const int st = kseq % kStages, pb = pseq % kPBufs;
-        const uint32_t pph = (pseq / kPBufs) & 1;
-        WAITC(&bars->full[st], (kseq / kStages) & 1, 21);
-        if (lane == 0) mbar_arrive_expect_tx(&bars->p_full[pb], kPBufBytes);
-        __syncwarp();
-        WAITC(&bars->p_full[pb], pph, 22);
-        WAIT(&bars->corr_done[pb], pph, 23);
+      WAITC(&bars->o_free, (oitem & 1) ^ 1, 20);
+      for (int j = 0; j < nt; ++j, ++kseq) {
+        const int st = kseq % kStages, pb = kseq % kPBufs;
+        const uint32_t kph = (kseq / kStages) & 1, pph = (kseq / kPBufs) & 1;
+        WAIT(&bars->full[st], kph, 21);
+        WAITC(&bars->peer[st], kph, 22);
+        WAITC(&bars->corr[pb], pph, 23);
         fence_after_sync();
         if (lane == 0) {
           const uint64_t adesc0 = smem_desc_sw128(smem_u32(pbufs + pb * kPBufBytes), 16, 1024);
-          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kKTileBytes), kChunkBytes, 1024);
+          const uint64_t bdesc0 = smem_desc_sw128(smem_u32(tiles + st * kStageBytes), kOChunk, 1024);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
 #pragma unroll
-            for (int k = 0; k < kBlockN / 16; ++k)
-              mma_ss(tmem + kTmemO + 256 * h, adesc0 + (uint64_t)((k * 32) >> 4),
-                     bdesc0 + (uint64_t)(((4 * h) * kChunkBytes + k * 2048) >> 4), idesc,
-                     (j > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kTileN / 16; ++k)
+              mma2_ss(tmem + kTmemO + 256 * h, adesc0 + (uint64_t)(((k >> 2) * kPChunk + (k & 3) * 32) >> 4),
+                      bdesc0 + (uint64_t)(((2 * h) * kOChunk + k * 2048) >> 4), idesc,
+                      (j > 0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(&bars->empty[st]);
-          mma_commit_mc(&bars->p_empty[pb], 0x1);
-          mma_commit(&bars->o_ready[pb]);
+          mma2_commit_mc(&bars->empty[st], 0xC);
+          mma2_commit_mc(&bars->p_free[pb], 0x3);
+          mma2_commit_mc(&bars->o_ready[pb], 0xC);
         }
         __syncwarp();
       }
       ++oitem;
     }
   }
-  // ======================================================================= score CTA: softmax
-  else if (score_cta) {
-    const int q4 = warp & 3;                 // TMEM lane quadrant of this warp
-    const int r = 32 * q4 + lane;            // query row within the group
+  // ======================================================================= score pair: softmax
+  // Thread (row r, column half ch) owns entries [64ch, 64ch+64) of every tile.
+  else if (score_cta && warp < kRowWarps) {
+    const int q4 = warp & 3, ch = warp >> 2;
+    const int r = 32 * q4 + lane;            // query row within this CTA's half
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
-    uint32_t sseq = 0, pseq = 0, qitem = 0;
+    float* red = reinterpret_cast<float*>(smem + kOffRed);   // [slot][ch][128]
+    uint32_t sseq = 0, qitem = 0;
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
       if (nt == 0) continue;
-      const bool live = r < it.nrows;
-      // Q rows of the item -> TMEM (A operand layout: lane = row, two bf16 per column).
-      WAIT(&bars->q_free, (qitem & 1) ^ 1, 30);
+      const int hrow0 = it.row0 + kHalfRows * half;
+      const int hrows = it.nrows - kHalfRows * half;
+      const bool live = r < hrows;
+      // Q rows of this half -> TMEM (A operand layout: lane = row, two bf16 per
+      // column); column half 0 loads units [0, 40), half 1 units [40, 72).
+      WAITC(&bars->q_free, (qitem & 1) ^ 1, 30);
+      if (warp == 0 && lane == 0) prefetch_q_rows(p, item_of(r_ + 1, cluster, n_clusters), n_items, half);
       fence_after_sync();
       {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                          (it.q_row_base + it.row0 + (live ? r : 0)) * kDqk);
-        // 72 loads of 16 bytes per row: issue 24 at a time (three TMEM chunks) to
-        // overlap the global-memory latency.
-        for (int c0 = 0; c0 < 9; c0 += 3) {
-          uint4 u[24];
+                                                          (it.q_row_base + hrow0 + (live ? r : 0)) * kDqk);
+        const int c_beg = ch ? 5 : 0, c_end = ch ? 9 : 5;   // TMEM chunks of 32 columns (8 units)
+        for (int c0 = c_beg; c0 < c_end; ++c0) {
+          uint4 u[8];
 #pragma unroll
-          for (int k = 0; k < 24; ++k) u[k] = live ? __ldg(src + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 8; ++k) u[k] = live ? __ldg(src + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+          uint32_t v[32];
 #pragma unroll
-          for (int cc = 0; cc < 3; ++cc) {
-            uint32_t v[32];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              v[4 * k] = u[8 * cc + k].x;
-              v[4 * k + 1] = u[8 * cc + k].y;
-              v[4 * k + 2] = u[8 * cc + k].z;
-              v[4 * k + 3] = u[8 * cc + k].w;
-            }
-            tmem_st32(tmem + lane_addr + kTmemQ + 32 * (c0 + cc), v);
+          for (int k = 0; k < 8; ++k) {
+            v[4 * k] = u[k].x;
+            v[4 * k + 1] = u[k].y;
+            v[4 * k + 2] = u[k].z;
+            v[4 * k + 3] = u[k].w;
           }
+          tmem_st32(tmem + lane_addr + kTmemQ + 32 * c0, v);
         }
         tmem_wait_st();
       }
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->q_full);
+      if (lane == 0) arrive_at(&bars->q_full, lead, rank);
       ++qitem;
 
       // Visibility: local entry i is visible to this row iff ibeg <= i < iend, its
       // index is valid and, with per-entry positions, its position passes the
       // row's causal limit (and window).
-      const int t_row = (it.row0 + r) / p.num_heads;
+      const int t_row = (hrow0 + r) / p.num_heads;
       int ibeg = 0, iend = it.e1;
       if (p.causal && live && !p.kv_pos) {
         const int64_t lim = it.Lg - it.T + t_row - it.base;
@@ -517,71 +654,80 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
       }
       if (!live) iend = -1;
       // tokens of this warp's 32 rows (per-entry positions need one mask per token)
-      const int t_first = (it.row0 + 32 * q4) / p.num_heads, t_last = (it.row0 + 32 * q4 + 31) / p.num_heads;
+      const int t_first = (hrow0 + 32 * q4) / p.num_heads, t_last = (hrow0 + 32 * q4 + 31) / p.num_heads;
       float m_ref = -INFINITY, l = 0.f;
-      for (int j = 0; j < nt; ++j, ++sseq, ++pseq) {
-        const int sb = sseq & 1, pb = pseq % kPBufs;
-        const int i0 = it.e0 + j * kBlockN;
-        // validity of the tile's 64 slot indices
-        uint32_t vlo, vhi;
+      for (int j = 0; j < nt; ++j, ++sseq) {
+        const int pb = sseq % kPBufs;
+        const int i0 = it.e0 + j * kTileN + 64 * ch;   // first entry of this thread's 64
+        // validity of the 64 slot indices: word w covers entries i0 + 32w ..
+        uint32_t vm[2];
         {
-          const int a = i0 + lane, b = a + 32;
-          bool ok0 = false, ok1 = false;
-          if (a < it.e1) {
-            const int32_t s = __ldg(p.kv_indices + it.kv_off + a);
-            ok0 = s >= 0 && s < p.num_slots;
-          }
-          if (b < it.e1) {
-            const int32_t s = __ldg(p.kv_indices + it.kv_off + b);
-            ok1 = s >= 0 && s < p.num_slots;
+          bool ok[2];
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const int a = i0 + 32 * w + lane;
+            ok[w] = false;
+            if (a < it.e1) {
+              const int32_t s = __ldg(p.kv_indices + it.kv_off + a);
+              ok[w] = s >= 0 && s < p.num_slots;
+            }
           }
           if (p.kv_pos && p.causal) {
-            const int64_t g0 = a < it.e1 ? (int64_t)__ldg(p.kv_pos + it.kv_off + a) : INT64_MAX;
-            const int64_t g1 = b < it.e1 ? (int64_t)__ldg(p.kv_pos + it.kv_off + b) : INT64_MAX;
-            vlo = vhi = 0;
+            int64_t gp[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+              const int a = i0 + 32 * w + lane;
+              gp[w] = a < it.e1 ? (int64_t)__ldg(p.kv_pos + it.kv_off + a) : INT64_MAX;
+              vm[w] = 0;
+            }
             for (int t = t_first; t <= t_last; ++t) {
               const int64_t lim = it.Lg - it.T + t;
-              const bool in0 = g0 <= lim && (p.window <= 0 || g0 > lim - p.window);
-              const bool in1 = g1 <= lim && (p.window <= 0 || g1 > lim - p.window);
-              const uint32_t m0 = __ballot_sync(0xffffffffu, ok0 && in0);
-              const uint32_t m1 = __ballot_sync(0xffffffffu, ok1 && in1);
-              if (t == t_row) {
-                vlo = m0;
-                vhi = m1;
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                const bool in = gp[w] <= lim && (p.window <= 0 || gp[w] > lim - p.window);
+                const uint32_t mk = __ballot_sync(0xffffffffu, ok[w] && in);
+                if (t == t_row) vm[w] = mk;
               }
             }
           } else {
-            vlo = __ballot_sync(0xffffffffu, ok0);
-            vhi = __ballot_sync(0xffffffffu, ok1);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) vm[w] = __ballot_sync(0xffffffffu, ok[w]);
+          }
+          // entries [ibeg, iend) may be visible: fold the range into the masks
+          const int nvis = iend - i0, nbeg = ibeg - i0;
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const int hi = min(max(nvis - 32 * w, 0), 32), lo = min(max(nbeg - 32 * w, 0), 32);
+            const uint32_t range = (hi >= 32 ? 0xffffffffu : ((1u << hi) - 1u)) & (lo >= 32 ? 0u : (0xffffffffu << lo));
+            vm[w] &= range;
           }
         }
-        WAIT(&bars->s_full[sb], (sseq >> 1) & 1, 31);
+        WAIT(&bars->s_full, sseq & 1, 31);
         fence_after_sync();
-        uint32_t s0[32], s1[32];
-        tmem_ld32(tmem + lane_addr + kTmemS + sb * kBlockN, s0);
-        tmem_ld32(tmem + lane_addr + kTmemS + sb * kBlockN + 32, s1);
+        uint32_t sv[2][32];
+        tmem_ld32(tmem + lane_addr + kTmemS + 64 * ch, sv[0]);
+        tmem_ld32(tmem + lane_addr + kTmemS + 64 * ch + 32, sv[1]);
         tmem_wait_ld();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+        if (lane == 0) arrive_at(&bars->s_free, lead, rank);
 
-        // entries [nbeg, nvis) of the tile may be visible: fold the range into the masks
-        {
-          const int nvis = iend - i0, nbeg = ibeg - i0;
-          const int hi = nvis < 0 ? 0 : (nvis > 64 ? 64 : nvis), lo = nbeg < 0 ? 0 : (nbeg > 64 ? 64 : nbeg);
-          const uint64_t range = (hi >= 64 ? ~0ull : ((1ull << hi) - 1)) & (lo >= 64 ? 0ull : (~0ull << lo));
-          vlo &= (uint32_t)range;
-          vhi &= (uint32_t)(range >> 32);
-        }
-        float x[64];
-        float tmax = -INFINITY;
+        float pmax = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          const uint32_t bits = e < 32 ? s0[e] : s1[e - 32];
-          const bool vis = ((e < 32 ? vlo : vhi) >> (e & 31)) & 1u;
-          x[e] = vis ? __uint_as_float(bits) * p.scale_log2 : -INFINITY;
-          tmax = fmaxf(tmax, x[e]);
+        for (int w = 0; w < 2; ++w) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const bool vis = (vm[w] >> e) & 1u;
+            const float x = vis ? __uint_as_float(sv[w][e]) * p.scale_log2 : -INFINITY;
+            sv[w][e] = __float_as_uint(x);
+            pmax = fmaxf(pmax, x);
+          }
         }
+        // the row's max over both halves
+        const int slot = sseq & 1;
+        red[(slot * 2 + ch) * kHalfRows + r] = pmax;
+        named_bar_sync(1 + q4, 64);
+        const float tmax = fmaxf(pmax, red[(slot * 2 + (ch ^ 1)) * kHalfRows + r]);
         float alpha = 1.f;
         int need = 0;
         if (tmax > m_ref + 8.f) {          // raise the reference max only when it grew a lot
@@ -589,112 +735,117 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
           m_ref = tmax;
           need = 1;
         }
-        float psum = 0.f;
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float a = m_ref == -INFINITY ? 0.f : ex2(x[e] - m_ref);
-          const float b = m_ref == -INFINITY ? 0.f : ex2(x[e + 1] - m_ref);
-          psum += a + b;
-          pk[e / 2] = pack_bf16x2(a, b);
-        }
-        l = l * alpha + psum;
         const int any_need = __any_sync(0xffffffffu, need);
-
-        // Hand P to the output CTA.
-        WAITC(&bars->p_empty[pb], ((pseq / kPBufs) & 1) ^ 1, 32);
+        // Hand P to the output CTA of this half.
+        WAITC(&bars->p_free[pb], ((sseq / kPBufs) & 1) ^ 1, 32);
         uint8_t* stg = pbufs + pb * kPBufBytes;
+        float psum = 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(stg + swz(r, u)) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int u = 0; u < 8; ++u) {      // 8 entries per 16-byte unit of chunk ch
+          uint32_t pk[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int e = 8 * u + 2 * q;
+            const float x0 = __uint_as_float(sv[e >> 5][e & 31]), x1 = __uint_as_float(sv[e >> 5][(e & 31) + 1]);
+            const float a = m_ref == -INFINITY ? 0.f : ex2(x0 - m_ref);
+            const float b = m_ref == -INFINITY ? 0.f : ex2(x1 - m_ref);
+            psum += a + b;
+            pk[q] = pack_bf16x2(a, b);
+          }
+          *reinterpret_cast<uint4*>(stg + ch * kPChunk + swz(r, u)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        l = l * alpha + psum;              // this half's share of the row sum
         float* stats = reinterpret_cast<float*>(stg + kPStatsOff);
-        stats[r] = alpha;
-        stats[128 + r] = m_ref;
-        stats[256 + r] = l;
-        if (lane == 0) reinterpret_cast<int*>(stats + 384)[q4] = any_need;
+        if (ch == 0) {
+          stats[r] = alpha;
+          stats[128 + r] = m_ref;
+          if (lane == 0) reinterpret_cast<int*>(stats + 512)[q4] = any_need;
+        }
+        stats[256 + 128 * ch + r] = l;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->p_ready[pb]);
-        if (warp == kWarpRow0) {
-          WAIT(&bars->p_ready[pb], (pseq / kPBufs) & 1, 34);
+        if (warp == 0) {
+          WAIT(&bars->p_ready[pb], (sseq / kPBufs) & 1, 34);
           if (lane == 0) {
             const uint32_t src = smem_u32(stg);
-            bulk_copy_to_peer(mapa(src, 1), src, kPBufBytes, mapa(smem_u32(&bars->p_full[pb]), 1));
+            bulk_copy_to_peer(mapa(src, out_peer), src, kPCopyBytes, mapa(smem_u32(&bars->p_full[pb]), out_peer));
           }
           __syncwarp();
         }
       }
     }
-    // Drain: the peer's last PV arrivals on p_empty must land before this CTA exits.
-    for (int k = 0; k < kPBufs && (int)pseq - 1 - k >= 0; ++k) {
-      const uint32_t s = pseq - 1 - k;
-      WAITC(&bars->p_empty[s % kPBufs], (s / kPBufs) & 1, 33);
+    // Drain: the output pair's last PV commits on p_free must land before this CTA exits.
+    for (int k = 0; k < kPBufs && (int)sseq - 1 - k >= 0; ++k) {
+      const uint32_t s = sseq - 1 - k;
+      WAITC(&bars->p_free[s % kPBufs], (s / kPBufs) & 1, 33);
     }
   }
-  // ======================================================================= output CTA: correction + epilogue
-  else {
-    const int q4 = warp & 3;
+  // ======================================================================= output pair: correction + epilogue
+  // Thread (row r, column half ch) owns O columns [256ch, 256ch+256).
+  else if (!score_cta && warp < kRowWarps) {
+    const int q4 = warp & 3, ch = warp >> 2;
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
+    uint8_t* epi = smem + (warp < 4 ? kOffEpi0 : kOffEpi1) + (warp & 3) * 2048;
+    float* wts = reinterpret_cast<float*>(smem + kOffEpi0);   // merge weights [S][128], 8 KB
     uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0, mrg_d_ph = 0;
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       if (!it.ok) continue;
       const int nt = item_tiles(it);
-      const bool live = r < it.nrows;
+      const int hrows = min(max(it.nrows - kHalfRows * half, 0), kHalfRows);
+      const bool live = r < hrows;
       float m_last = -INFINITY, l_last = 0.f;
       for (int j = 0; j < nt; ++j, ++pseq) {
         const int pb = pseq % kPBufs;
         const uint32_t pph = (pseq / kPBufs) & 1;
+        if (warp == 0 && lane == 0) mbar_arrive_expect_tx(&bars->p_full[pb], kPCopyBytes);
         WAITC(&bars->p_full[pb], pph, 40);
-        const uint8_t* pbuf = pbufs + pb * kPBufBytes;
-        const float* stats = reinterpret_cast<const float*>(pbuf + kPStatsOff);
-        const int* flags = reinterpret_cast<const int*>(stats + 384);
+        const float* stats = reinterpret_cast<const float*>(pbufs + pb * kPBufBytes + kPStatsOff);
         const float alpha = stats[r];
         m_last = stats[128 + r];
-        l_last = stats[256 + r];
-        if (flags[q4] && j > 0) {
+        l_last = stats[256 + r] + stats[384 + r];
+        if (reinterpret_cast<const int*>(stats + 512)[q4] && j > 0) {
           // O of the previous tile must be complete before rescaling it.
           const uint32_t prev = pseq - 1;
-          WAIT(&bars->o_ready[prev % kPBufs], (prev / kPBufs) & 1, 41);
+          WAITC(&bars->o_ready[prev % kPBufs], (prev / kPBufs) & 1, 41);
           fence_after_sync();
-          for (int c = 0; c < kDv / 32; ++c) {
+          for (int c = 0; c < 8; ++c) {
             uint32_t v[32];
-            tmem_ld32(tmem + lane_addr + kTmemO + 32 * c, v);
+            const uint32_t col = kTmemO + 256 * ch + 32 * c;
+            tmem_ld32(tmem + lane_addr + col, v);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * alpha);
-            tmem_st32(tmem + lane_addr + kTmemO + 32 * c, v);
+            tmem_st32(tmem + lane_addr + col, v);
           }
           tmem_wait_st();
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->corr_done[pb]);
+        if (lane == 0) arrive_at(&bars->corr[pb], lead, rank);
       }
       // Epilogue.
       const bool any = l_last > 0.f;
       const float inv = any ? p.out_scale / l_last : 0.f;
       const float lse = any ? (m_last + __log2f(l_last)) * 0.69314718055994531f : -INFINITY;
-      float* dst_f32 = nullptr;
-      const int64_t row = it.q_row_base + it.row0 + r;
-      if (it.slot >= 0) dst_f32 = p.part_o + ((int64_t)it.slot * kRows + r) * kDv;
-      else if (p.out_fp32) dst_f32 = static_cast<float*>(p.o) + row * kDv;
+      const int64_t irow = kHalfRows * half + r;             // row within the item
+      const int64_t row = it.q_row_base + it.row0 + irow;
+      const bool f32 = it.slot >= 0 || p.out_fp32;
       if (nt > 0) {
         const uint32_t last = pseq - 1;
-        WAIT(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
+        WAITC(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
         fence_after_sync();
       }
-      // O[row = lane][32 columns] per step: staged in this warp's 4 KB (128-byte
-      // row pitch, 16-byte units XOR-swizzled by row) and written back as whole
-      // row segments, 128 (fp32) or 64 (bf16) contiguous bytes per row.
-      uint8_t* stg = smem + kOffEpi + (warp - kWarpRow0) * 4096;
-      const bool f32 = dst_f32 != nullptr;
-      for (int c = 0; c < kDv / 32; ++c) {
+      // O[row = lane][32 columns] per step, staged in this warp's 2 KB as 64-byte
+      // row segments (32 bf16 or 2 x 16 fp32 columns) and written back whole.
+      for (int c = 0; c < 8; ++c) {
+        const int col = 256 * ch + 32 * c;
         float v[32];
         if (nt > 0) {
           uint32_t u[32];
-          tmem_ld32(tmem + lane_addr + kTmemO + 32 * c, u);
+          tmem_ld32(tmem + lane_addr + kTmemO + col, u);
           tmem_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(u[k]) * inv;
@@ -704,42 +855,47 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
         }
         if (f32) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            *reinterpret_cast<float4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
-                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<float4*>(epi + swz64(lane, k)) =
+                  make_float4(v[16 * hh + 4 * k], v[16 * hh + 4 * k + 1], v[16 * hh + 4 * k + 2], v[16 * hh + 4 * k + 3]);
+            __syncwarp();
+            epi_rows_out(epi, lane, q4, col + 16 * hh, true, it, half, hrows, p);
+            __syncwarp();
+          }
         } else {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(stg + lane * 128 + ((k ^ (lane & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(epi + swz64(lane, k)) =
                 make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
                            pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+          __syncwarp();
+          epi_rows_out(epi, lane, q4, col, false, it, half, hrows, p);
+          __syncwarp();
         }
-        __syncwarp();
-        if (f32) epi_rows_out<true>(stg, lane, q4, c, it, p);
-        else epi_rows_out<false>(stg, lane, q4, c, it, p);
-        __syncwarp();
       }
-      if (live) {
-        if (it.slot >= 0) p.part_lse[(int64_t)it.slot * kRows + r] = lse;
+      if (live && ch == 0) {
+        if (it.slot >= 0) p.part_lse[(int64_t)it.slot * kRows + irow] = lse;
         else p.lse[row] = lse;
       }
       if (nt > 0) {
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->o_free);
+        if (lane == 0) arrive_at(&bars->o_free, lead, rank);
       }
-      if (it.slot >= 0) {
-        // Fused split merge: the last split of this (request, row group) to finish
-        // combines every split's partial in split order.  The 4 row warps first
-        // agree (leader counts one arrival per split), then merge together.
+      if (it.slot >= 0 && hrows > 0) {
+        // Fused split merge of this half: the last split of this (request, row
+        // group) to finish combines every split's partial rows in split order.
+        // The row warps first agree (warp 0 counts one arrival per split), then
+        // merge together.
         __threadfence();
-        fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->mrg_a);
-        if (warp == kWarpRow0) {
+        if (warp == 0) {
           WAIT(&bars->mrg_a, mrg_a_ph, 43);
           if (lane == 0) {
-            bars->merge_last = atomicAdd(&p.counters[it.group], 1) == it.S - 1;
+            bars->merge_last = atomicAdd(&p.counters[2 * it.group + half], 1) == it.S - 1;
             mbar_arrive(&bars->mrg_b);
           }
           __syncwarp();
@@ -752,47 +908,46 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
           const int B = p.batch;
           const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
           const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
-          // pass 1 (thread = row): max, normaliser and the weight of every split,
-          // kept in the epilogue staging area as w[s][row]
-          float* wts = reinterpret_cast<float*>(smem + kOffEpi);
-          {
+          // pass 1 (column half 0, thread = row): max, normaliser and the weight of every split
+          if (ch == 0) {
             float M = -INFINITY;
             if (live)
               for (int s = 0; s < it.S; ++s)
-                M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r));
+                M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow));
             float tot = 0.f;
             if (M != -INFINITY)
               for (int s = 0; s < it.S; ++s) {
-                const float ls = __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + r);
+                const float ls = __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
                 const float e = ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
-                wts[s * kRows + r] = e;
+                wts[s * kHalfRows + r] = e;
                 tot += e;
               }
-            const float inv = M == -INFINITY ? 0.f : 1.f / tot;
-            for (int s = 0; s < it.S; ++s) wts[s * kRows + r] = M == -INFINITY ? 0.f : wts[s * kRows + r] * inv;
+            const float winv = M == -INFINITY ? 0.f : 1.f / tot;
+            for (int s = 0; s < it.S; ++s)
+              wts[s * kHalfRows + r] = M == -INFINITY ? 0.f : wts[s * kHalfRows + r] * winv;
             if (live) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->mrg_c);
           WAIT(&bars->mrg_c, mrg_c_ph, 45);
           mrg_c_ph ^= 1;
-          // pass 2: thread t owns float4 column t of every row; 16 rows in flight
-          const int c4 = tid - kWarpRow0 * 32;
-          for (int rb = 0; rb < it.nrows; rb += 16) {
-            float4 acc[16];
+          // pass 2: thread t owns float4 column t % 128 of rows of parity t / 128; 8 rows in flight
+          const int c4 = tid & 127, rsub = tid >> 7;
+          for (int rb = 0; rb < hrows; rb += 16) {
+            float4 acc[8];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int s = 0; s < it.S; ++s) {
               const int slot = pbase + s * G + it.g;
-              float4 ov[16];
+              float4 ov[8];
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int rr = min(rb + k, it.nrows - 1);
+              for (int k = 0; k < 8; ++k) {
+                const int rr = kHalfRows * half + min(rb + 2 * k + rsub, hrows - 1);
                 ov[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + rr) * kDv) + c4);
               }
 #pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const float w = wts[s * kRows + min(rb + k, it.nrows - 1)];
+              for (int k = 0; k < 8; ++k) {
+                const float w = wts[s * kHalfRows + min(rb + 2 * k + rsub, hrows - 1)];
                 acc[k].x += w * ov[k].x;
                 acc[k].y += w * ov[k].y;
                 acc[k].z += w * ov[k].z;
@@ -800,9 +955,10 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
               }
             }
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              if (rb + k >= it.nrows) break;
-              const int64_t orow = it.q_row_base + it.row0 + rb + k;
+            for (int k = 0; k < 8; ++k) {
+              const int rl = rb + 2 * k + rsub;
+              if (rl >= hrows) break;
+              const int64_t orow = it.q_row_base + it.row0 + kHalfRows * half + rl;
               if (p.out_fp32) {
                 reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * kDv)[c4] = acc[k];
               } else {
@@ -813,7 +969,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
               }
             }
           }
-          if (tid == kWarpRow0 * 32) p.counters[it.group] = 0;
+          if (tid == 0) p.counters[2 * it.group + half] = 0;
           // the weights live where the next epilogue stages its rows
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->mrg_d);
@@ -827,8 +983,9 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_kv, const Deco
 done:
   fence_before_sync();
   __syncthreads();
-  if (warp == kWarpMma) tmem_dealloc(tmem, 512);
-  cluster_sync();
+  cluster_sync();        // the pairs' MMAs and every remote arrival are finished
+  fence_after_sync();
+  if (warp == kWarpMma) tmem_dealloc2(tmem, 512);
 }
 
 // ----------------------------------------------------------------------- host side
@@ -850,44 +1007,54 @@ EncodeTiledFn get_encode() {
   return fn;
 }
 
-template <bool kFp8>
-mla_status launch_impl(const DecodeParams& dp, void* stream) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return MLA_ERR_CUDA;
-  CUtensorMap tmap;
+// Row-gather tensor map over the pool: one row high, `box` elements wide.
+bool encode_pool_map(EncodeTiledFn enc, CUtensorMap* tm, const DecodeParams& dp, bool fp8, uint32_t box) {
   const cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)dp.num_slots};
-  const cuuint64_t gstride[1] = {(cuuint64_t)kDqk * (kFp8 ? 1 : 2)};
-  const cuuint32_t box[2] = {kFp8 ? 192u : 64u, 1u};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kDqk * (fp8 ? 1 : 2)};
+  const cuuint32_t boxd[2] = {box, 1u};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = enc(&tmap, kFp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void*>(dp.kv), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return MLA_ERR_INVALID_ARG;
-  const int smem = kSmemBytes + kSmemAlign;
-  auto kern = mla_decode_tensor_kernel<kFp8>;
-  static int max_clusters[kMaxDevices][2] = {};
-  const int dev = current_device_slot();
-  if (dev < 0) return MLA_ERR_CUDA;
-  if (max_clusters[dev][kFp8] == 0) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return MLA_ERR_CUDA;
+  return enc(tm, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+             const_cast<void*>(dp.kv), gdim, gstride, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Clusters of this kernel that fit on the device at once (cached per device).
+template <bool kFp8>
+int max_active_clusters(int dev) {
+  static int cache[kMaxDevices] = {0};
+  if (dev < 0) return 0;
+  if (cache[dev] == 0) {
+    const int smem = kSmemBytes + kSmemAlign;
+    auto kern = mla_decode_tensor_kernel<kFp8>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(threads_for(kFp8), 1, 1);
+    cfg.gridDim = dim3(4, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.x = 4;
     attr.val.clusterDim.y = 1;
     attr.val.clusterDim.z = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return MLA_ERR_CUDA;
-    max_clusters[dev][kFp8] = n;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return 0;
+    cache[dev] = n;
   }
-  int clusters = max_clusters[dev][kFp8];
+  return cache[dev];
+}
+
+template <bool kFp8>
+mla_status launch_impl(const DecodeParams& dp, void* stream) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MLA_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if (!encode_pool_map(enc, &tk, dp, kFp8, kFp8 ? 192u : 64u)) return MLA_ERR_INVALID_ARG;
+  if (!encode_pool_map(enc, &tv, dp, kFp8, kFp8 ? 128u : 64u)) return MLA_ERR_INVALID_ARG;
+  int clusters = max_active_clusters<kFp8>(current_device_slot());
+  if (clusters < 1) return MLA_ERR_CUDA;
   if (clusters > dp.items_cap) clusters = dp.items_cap > 0 ? dp.items_cap : 1;
   DecodeParams kp = dp;
   if (kFp8) {
@@ -895,13 +1062,20 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
     kp.scale_log2 = dp.scale_log2 * 5.192296858534828e33f;
     kp.out_scale = dp.out_scale * 5.192296858534828e33f;
   }
-  kern<<<2 * clusters, threads_for(kFp8), smem, (cudaStream_t)stream>>>(tmap, kp);
+  mla_decode_tensor_kernel<kFp8>
+      <<<4 * clusters, kThreads, kSmemBytes + kSmemAlign, (cudaStream_t)stream>>>(tk, tv, kp);
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
 
 int tensor_kernel_available() { return 1; }
+
+int tensor_kernel_workers() {
+  const int dev = current_device_slot();
+  const int a = max_active_clusters<false>(dev), b = max_active_clusters<true>(dev);
+  return a < b ? a : b;
+}
 
 mla_status launch_decode_tensor(const DecodeParams& dp, void* stream) {
   return dp.kv_fp8 ? launch_impl<true>(dp, stream) : launch_impl<false>(dp, stream);

@@ -50,9 +50,9 @@ inline PlanGeom plan_geom(const mla_plan_params& p) {
 // ---------------------------------------------------------------- workspace layout
 // [0, 256)       header words: 0 error code, 1 error info (both persist until read),
 //                2.. per-call state (queue heads), zeroed at the start of every call
-// counters       int32 [B * g_max]      split-merge arrival counters per (b, g)
-// part_lse       fp32 [items_cap, 128]
-// part_o         fp32 [items_cap, 128, 512]
+// counters       int32 [2 * B * g_max]  split-merge arrival counters per (b, g, row half)
+// part_lse       fp32 [items_cap, 256]
+// part_o         fp32 [items_cap, 256, 512]
 enum WsHeader : int { kWsErrCode = 0, kWsErrInfo = 1, kWsQueue = 2, kWsQueue2 = 3 };
 
 struct WsGeom {
@@ -65,7 +65,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline WsGeom ws_geom(const mla_plan_params& p) {
   PlanGeom pg = plan_geom(p);
   WsGeom w;
-  w.counters_cap = (int64_t)p.batch * pg.g_max;
+  w.counters_cap = 2 * (int64_t)p.batch * pg.g_max;
   if (w.counters_cap < 1) w.counters_cap = 1;
   w.partial_cap = pg.items_cap;
   w.counters_off = 256;
@@ -96,6 +96,8 @@ struct DecodeParams {
   void* o;
   float* lse;
   const int32_t* plan;
+  long long wait_limit;  // cycles a barrier wait may take before it reports MLA_DEV_WAIT_TIMEOUT
+  int32_t test_stall;    // failure-path test: wait on a barrier nothing signals before any work
   int32_t* ws_hdr;
   int32_t* counters;
   float* part_lse;
@@ -120,6 +122,7 @@ mla_status launch_cache_write(const mla_cache_write_args& a, void* stream);
 mla_status launch_rope_q_cache(const mla_rope_q_cache_args& a, void* stream);
 mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream);
 int tensor_kernel_available();
+int tensor_kernel_workers();   // clusters of the tensor kernel resident at once (0 on error)
 
 // Launch-time facts cached per device (opt-in shared-memory sizes, SM counts,
 // occupancy): cudaFuncSetAttribute and the SM count belong to one device, so the

@@ -7,19 +7,22 @@ from typing import Optional
 import numpy as np
 
 from . import (MLA_ALGO_TENSOR, MLA_PLAN_DYNAMIC, MLA_PLAN_HOST, MLA_PLAN_STATIC, mla_decode_fwd,
-               mla_decode_plan, mla_decode_plan_size, plan_params)
+               mla_decode_plan, mla_decode_plan_size, mla_decode_workers, plan_params)
 
 
-def default_workers(device=None) -> int:
+def default_workers(device=None, algo: int = MLA_ALGO_TENSOR) -> int:
+    """Work items the decode kernel runs at once on the device: the plan splits
+    long rows to give about this many items."""
     import torch
-    return int(torch.cuda.get_device_properties(device or torch.cuda.current_device()).multi_processor_count)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        return mla_decode_workers(algo)
 
 
 def default_workers_for(algo: int, batch: int, num_heads: int, max_q_len: int, device=None) -> int:
-    """Plan workers for a shape: the tensor kernel runs one work item per CTA
-    pair, so one worker per pair of SMs; the CUDA-core kernel one per SM."""
-    sms = default_workers(device)
-    return sms // 2 if algo == MLA_ALGO_TENSOR else sms
+    """Plan workers for a shape: the tensor kernel runs one work item per
+    four-SM cluster, the CUDA-core kernel one per SM."""
+    return default_workers(device, algo)
 
 
 class DecodeRunner:
