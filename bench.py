@@ -11,9 +11,10 @@ of the shards) over one batch of synthetic input already resident in HBM.
 The other configs time the steps either side of the decode, each on its own
 (tokens per second, HBM roofline): cache_write_fp8 / cache_write_bf16 (KV-cache
 write), rope_cache_fp8 (fused RoPE + q concat + cache write) and absorb_bmm_fp8
-(absorb and un-absorb BMMs).  Between timed steps the L2 is flushed (a 256 MB
-write, then another 256 MB read); the timed steps are queued behind a bounded GPU
-spin so host launch cost does not sit inside the CUDA events.
+(absorb and un-absorb BMMs).  Every step is one replay of a captured CUDA graph,
+timed by event record nodes inside the graph (the median over the steps is
+reported); between replays the L2 is flushed (a 256 MB write, then another
+256 MB read).
 
 Under torchrun (N > 1) every rank decodes its own batch of the same shape (requests
 are independent: weak scaling, no collective on the data path); rank 0 prints the
@@ -131,15 +132,6 @@ class L2Flush:
 
 
 L2_NOTE = "flushed between timed steps (256 MB written, then another 256 MB read)"
-
-
-def queue_ahead(torch, steps: int, host_us_per_step: float = 250.0):
-    """Hold the GPU in a bounded spin while the host enqueues the timed steps, so
-    the host's per-call cost (argument checks, tensor-map encoding, launches) does
-    not appear as idle gaps inside the event-timed regions: the events then bracket
-    device work only.  The spin ends by itself after about host_us_per_step per step."""
-    if hasattr(torch.cuda, "_sleep"):
-        torch.cuda._sleep(int(2000 * host_us_per_step * min(steps, 2000)))
 
 
 def load_peaks():
@@ -349,21 +341,12 @@ def cache_write_main(args, rank: int, world: int):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev_index) as clk:
-        queue_ahead(torch, args.steps)
-        for i in range(args.steps):
-            flush()
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
+    times, clocks = graph_timed(torch, [step], args.steps, flush, dev_index)
     if world > 1:
         torch.distributed.barrier()
-    ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world, device="cuda")
+    ms = slowest_rank_ms(statistics.median(t[0] for t in times), world, device="cuda")
     # end to end: the step's activations and slots from pinned host memory, the
     # write, and one written row read back as the completion check
     kc_h, kp_h, sl_h = kv_c.cpu().pin_memory(), k_pe.cpu().pin_memory(), slots.cpu().pin_memory()
@@ -405,14 +388,15 @@ def cache_write_main(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16->" + kv_dtype, "data": "synthetic",
         "config": {"workload": args.config, "tokens": CW_TOKENS, "pool_slots": CW_SLOTS, "kv_dtype": kv_dtype,
-                   "l2": L2_NOTE},
+                   "l2": L2_NOTE,
+                   "timing": f"median of {args.steps} CUDA-graph replays"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "peak_source": peaks["source"],
                      "alg_bytes": nbytes},
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(CW_TOKENS, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps, "clocks": clk.summary()}))
+        "gpu_launches": args.steps, "clocks": clocks}))
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -481,21 +465,12 @@ def rope_cache_main(args, rank: int, world: int):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev_index) as clk:
-        queue_ahead(torch, args.steps)
-        for i in range(args.steps):
-            flush()
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        torch.cuda.synchronize()
+    times, clocks = graph_timed(torch, [step], args.steps, flush, dev_index)
     if world > 1:
         torch.distributed.barrier()
-    ms = slowest_rank_ms(sum(a.elapsed_time(b) for a, b in evs) / args.steps, world, device="cuda")
+    ms = slowest_rank_ms(statistics.median(t[0] for t in times), world, device="cuda")
     # end to end: the step's activations, positions and slots from pinned host memory,
     # the fused call, and q read back (it is what the decode consumes next)
     hosts = [t.cpu().pin_memory() for t in (q_nope, q_pe, kv_c, k_pe, pos, slots)]
@@ -536,14 +511,14 @@ def rope_cache_main(args, rank: int, world: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16/f32-rope->fp8", "data": "synthetic",
         "config": {"workload": args.config, "tokens": RC_TOKENS, "heads": RC_HEADS, "pool_slots": RC_SLOTS,
-                   "rope": "neox", "l2": L2_NOTE},
+                   "rope": "neox", "l2": L2_NOTE, "timing": f"median of {args.steps} CUDA-graph replays"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic(args.config, "ncu_traffic_cache_write.json"),
                      "peak_source": peaks["source"], "alg_bytes": nbytes},
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(RC_TOKENS, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps, "clocks": clk.summary()}))
+        "gpu_launches": args.steps, "clocks": clocks}))
     if world > 1:
         torch.distributed.destroy_process_group()
 
@@ -617,25 +592,14 @@ def absorb_main(args, rank: int, world: int):
         absorb()
         unabsorb()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev_index) as clk:
-        queue_ahead(torch, args.steps)
-        for i in range(args.steps):
-            flush()
-            ev[i][0].record(stream)
-            absorb()
-            ev[i][1].record(stream)
-            unabsorb()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
+    times, clocks = graph_timed(torch, [absorb, unabsorb], args.steps, flush, dev_index)
     if world > 1:
         torch.distributed.barrier()
-    ms_a = sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps
-    ms_u = sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps
-    ms = slowest_rank_ms(ms_a + ms_u, world, device="cuda")
+    ms_a = statistics.median(t[0] for t in times)
+    ms_u = statistics.median(t[1] for t in times)
+    ms = slowest_rank_ms(statistics.median(t[0] + t[1] for t in times), world, device="cuda")
     # end to end: q_nope and the decode output from pinned host memory, both BMMs,
     # the 576-wide q and the un-absorbed output read back
     hosts = [t.cpu().pin_memory() for t in (q_nope, o_lat)]
@@ -681,7 +645,7 @@ def absorb_main(args, rank: int, world: int):
         "config": {"workload": args.config, "tokens": AB_TOKENS, "heads": AB_HEADS,
                    "absorb": "q_nope[256,128,128] @ W_UK[128,128,512] -> q[..., :512]",
                    "unabsorb": "o_lat[256,128,512] @ W_UV[128,512,128]",
-                   "l2": L2_NOTE},
+                   "l2": L2_NOTE, "timing": f"median of {args.steps} CUDA-graph replays"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": ncu_traffic(key, "ncu_traffic_absorb_bmm.json"),
                      "peak_source": peaks["source"], "alg_bytes": nbytes, "kernel": f"mla_absorb_bmm ({dominant})",
@@ -690,9 +654,64 @@ def absorb_main(args, rank: int, world: int):
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(AB_TOKENS, world, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps, "clocks": clk.summary()}))
+        "gpu_launches": 2 * args.steps, "clocks": clocks}))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- graph-replay timing
+
+def graph_timed(torch, parts, steps: int, flush, dev_index: int, before_step=None):
+    """Capture `parts` (callables enqueuing device work) as one CUDA graph with a
+    timing event before, between and after them, then replay it `steps` times,
+    flushing the L2 (and running before_step(i), untimed) ahead of each replay.
+    Returns (per-step lists of part durations in ms, clock summary).  The events
+    are record nodes inside the graph, so they bracket device work only; without
+    external events in this torch they are recorded around the replay instead."""
+    evs = _timing_events_n(torch, len(parts) + 1)
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream()
+    cap_stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap_stream):
+        for f in parts:
+            f()
+    cap_stream.synchronize()
+    inside = evs is not None
+    with torch.cuda.graph(graph, stream=cap_stream):
+        for k, f in enumerate(parts):
+            if inside:
+                evs[k].record()
+            f()
+        if inside:
+            evs[len(parts)].record()
+    if not inside:
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+    out = []
+    torch.cuda.synchronize()
+    with ClockSampler(dev_index) as clk:
+        for i in range(steps):
+            if before_step is not None:
+                before_step(i)
+            flush()
+            if not inside:
+                evs[0].record(stream)
+            graph.replay()
+            if not inside:
+                evs[1].record(stream)
+            torch.cuda.synchronize()
+            if inside:
+                out.append([evs[k].elapsed_time(evs[k + 1]) for k in range(len(parts))])
+            else:
+                out.append([evs[0].elapsed_time(evs[1])] + [0.0] * (len(parts) - 1))
+    return out, clk.summary()
+
+
+def _timing_events_n(torch, n):
+    try:
+        return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+    except TypeError:
+        return None
 
 
 # ----------------------------------------------------------------------------- decode
@@ -718,15 +737,6 @@ def roofline_of(flops: float, nbytes: float, seconds: float, peaks: dict) -> dic
         out.update(bound="hbm", achieved=gbs, peak=peaks["hbm_gbs"], unit="GB/s",
                    frac=gbs / peaks["hbm_gbs"])
     return out
-
-
-def _timing_events(torch):
-    """Timing events that can be recorded inside a captured graph (event record
-    nodes); None where this torch has no external events."""
-    try:
-        return [torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)]
-    except TypeError:
-        return None
 
 
 def decode_main(args, rank: int, world: int):
@@ -815,54 +825,20 @@ def decode_main(args, rank: int, world: int):
     code, info = m.mla_get_device_error(runner.workspace)
     assert code == 0, f"device error {code} ({info})"
 
-    # One captured graph per step: [event, decode call, event, merge, event].  The
-    # events are record nodes inside the graph, so they bracket device work only.
-    evs = _timing_events(torch)
-    graph = torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream()
-    cap_stream.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(cap_stream):
-        step()
-    cap_stream.synchronize()
-    with torch.cuda.graph(graph, stream=cap_stream):
-        if evs:
-            evs[0].record()
-        decode()
-        if evs:
-            evs[1].record()
-        merge()
-        if evs:
-            evs[2].record()
-    if evs is None:
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        outside = True
-    else:
-        outside = False
-    stream = torch.cuda.current_stream()
-
+    # One captured graph per step: [decode call, merge], timed by event record
+    # nodes inside the graph; long skewed contexts load a new draw before each replay.
     if world > 1:
         torch.distributed.barrier()
-    torch.cuda.synchronize()
-    step_ms, dec_ms, which = [], [], []
-    with ClockSampler(dev_index) as clk:
-        for i in range(args.steps):
-            r = i % len(replays)
-            if len(replays) > 1:
-                load(replays[r])          # new lengths, T and indices (not timed)
-            flush()                       # L2 flush between timed steps (not timed)
-            if outside:
-                evs[0].record(stream)
-            graph.replay()
-            if outside:
-                evs[2].record(stream)
-            torch.cuda.synchronize()
-            step_ms.append(evs[0].elapsed_time(evs[2]))
-            dec_ms.append(evs[0].elapsed_time(evs[1]) if not outside else step_ms[-1])
-            which.append(r)
+    before = (lambda i: load(replays[i % len(replays)])) if len(replays) > 1 else None
+    times, clocks = graph_timed(torch, [decode, merge], args.steps, flush, dev_index, before_step=before)
+    step_ms = [t[0] + t[1] for t in times]
+    dec_ms = [t[0] for t in times]
+    which = [i % len(replays) for i in range(args.steps)]
     code, info = m.mla_get_device_error(runner.workspace)
     assert code == 0, f"device error {code} ({info})"
     if world > 1:
         torch.distributed.barrier()
+    stream = torch.cuda.current_stream()
     rates = [units[r % len(units)] / (t * 1e-3) for t, r in zip(step_ms, which)]
     rate_med = statistics.median(rates)
     ms_med = statistics.median(step_ms)
@@ -941,7 +917,7 @@ def decode_main(args, rank: int, world: int):
             "e2e": {"value": whole_job_rate(units[0], world, e2e_ms), "unit": "KV-tokens*heads/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
         }
         print(json.dumps(line))
     if world > 1:

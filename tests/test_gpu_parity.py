@@ -170,9 +170,11 @@ def test_device_plan_bit_exact(seed):
 # ------------------------------------------------------------------ merge
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
-def test_merge_states_matches_oracle(dtype):
-    rng = np.random.default_rng(4)
-    n, rows, dv = 5, 777, 512
+@pytest.mark.parametrize("n,dv", [(5, 512), (12, 512), (3, 96)], ids=["n5", "n12", "dv96"])
+def test_merge_states_matches_oracle(dtype, n, dv):
+    """Both merge paths: vectorised (dv a multiple of 256, up to 8 or 16 states) and general."""
+    rng = np.random.default_rng(4 + n + dv)
+    rows = 777
     o = rng.standard_normal((n, rows, dv)).astype(np.float32)
     lse = (rng.standard_normal((n, rows)) * 3).astype(np.float32)
     lse[1, :100] = -np.inf

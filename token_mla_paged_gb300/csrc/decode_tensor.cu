@@ -127,10 +127,8 @@ struct Bars {
   uint64_t corr[kPBufs];      // output, even rank: both CTAs hold P and have rescaled O
   uint64_t o_ready[kPBufs];   // output: PV with this P buffer done
   uint64_t o_free;            // output, even rank: both epilogues read O
-  uint64_t mrg_a;             // output: the row warps fenced their partial rows
-  uint64_t mrg_b;             // output: leader published the last-arriver verdict
-  uint64_t mrg_c;             // output: per-row merge weights ready
-  uint64_t mrg_d;             // output: the row warps are done with the weights
+  uint64_t mrg_b;             // output: warp 0 published the split's verdict (partial / merge)
+  uint64_t mrg_c;             // output: the row warps fenced their partial rows
   uint64_t never;             // failure-path test: nothing ever arrives here
   uint32_t tmem_base;
   int abort;
@@ -226,10 +224,11 @@ __device__ __forceinline__ void fp8_unit_to_bf16(uint8_t* dst0, uint8_t* dst1, c
 }
 
 // Epilogue write-back of a 64-byte column segment (32 bf16 or 16 fp32 columns
-// starting at column `col`) of a warp's 32 rows, staged at stg as [32][64 B]:
-// each store instruction writes eight whole 64-byte row segments.
-__device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q4, int col, bool f32,
-                                             const Item& it, int half, int hrows, const DecodeParams& p) {
+// starting at byte `col_byte` of each row) of a warp's 32 rows, staged at stg as
+// [32][64 B]: each store instruction writes eight whole 64-byte row segments.
+// Row ri of this CTA's half lives at base + (128*half + ri) * pitch.
+__device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q4, int col_byte, uint8_t* base,
+                                             int64_t pitch, int half, int hrows) {
   uint4 val[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -240,14 +239,35 @@ __device__ __forceinline__ void epi_rows_out(const uint8_t* stg, int lane, int q
   for (int i = 0; i < 4; ++i) {
     const int rl = 8 * i + (lane >> 2), u = lane & 3;
     const int ri = 32 * q4 + rl;                 // row within this half
-    if (ri < hrows) {
-      const int64_t irow = kHalfRows * half + ri;   // row within the item
-      void* dst;
-      if (!f32) dst = static_cast<__nv_bfloat16*>(p.o) + (it.q_row_base + it.row0 + irow) * kDv + col + 8 * u;
-      else if (it.slot >= 0) dst = p.part_o + ((int64_t)it.slot * kRows + irow) * kDv + col + 4 * u;
-      else dst = static_cast<float*>(p.o) + (it.q_row_base + it.row0 + irow) * kDv + col + 4 * u;
-      *reinterpret_cast<uint4*>(dst) = val[i];
+    if (ri < hrows)
+      *reinterpret_cast<uint4*>(base + (int64_t)(kHalfRows * half + ri) * pitch + col_byte + 16 * u) = val[i];
+  }
+}
+
+// One thread's 32 values -> its row of the warp's staging block, then the warp
+// writes the block out (fp32: two 64-byte halves; bf16: one).
+__device__ __forceinline__ void stage_and_write(const float (&v)[32], bool f32, uint8_t* epi, int lane, int q4,
+                                                int col, uint8_t* base, int64_t pitch, int half, int hrows) {
+  if (f32) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float4*>(epi + swz64(lane, k)) =
+            make_float4(v[16 * hh + 4 * k], v[16 * hh + 4 * k + 1], v[16 * hh + 4 * k + 2], v[16 * hh + 4 * k + 3]);
+      __syncwarp();
+      epi_rows_out(epi, lane, q4, 4 * (col + 16 * hh), base, pitch, half, hrows);
+      __syncwarp();
     }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(epi + swz64(lane, k)) =
+          make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                     pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+    __syncwarp();
+    epi_rows_out(epi, lane, q4, 2 * col, base, pitch, half, hrows);
+    __syncwarp();
   }
 }
 
@@ -294,10 +314,8 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       mbar_init(&bars->o_ready[b], 1);
     }
     mbar_init(&bars->o_free, 2 * kRowWarps);
-    mbar_init(&bars->mrg_a, kRowWarps);
     mbar_init(&bars->mrg_b, 1);
     mbar_init(&bars->mrg_c, kRowWarps);
-    mbar_init(&bars->mrg_d, kRowWarps);
     mbar_init(&bars->never, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -788,8 +806,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
     const int r = 32 * q4 + lane;
     const uint32_t lane_addr = (uint32_t)(32 * q4) << 16;
     uint8_t* epi = smem + (warp < 4 ? kOffEpi0 : kOffEpi1) + (warp & 3) * 2048;
-    float* wts = reinterpret_cast<float*>(smem + kOffEpi0);   // merge weights [S][128], 8 KB
-    uint32_t pseq = 0, mrg_a_ph = 0, mrg_b_ph = 0, mrg_c_ph = 0, mrg_d_ph = 0;
+    uint32_t pseq = 0, mrg_b_ph = 0, mrg_c_ph = 0;
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       if (!it.ok) continue;
@@ -832,150 +849,182 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       const float lse = any ? (m_last + __log2f(l_last)) * 0.69314718055994531f : -INFINITY;
       const int64_t irow = kHalfRows * half + r;             // row within the item
       const int64_t row = it.q_row_base + it.row0 + irow;
-      const bool f32 = it.slot >= 0 || p.out_fp32;
+      // Split partials are bf16 unless the call wants fp32 output: O of a split is
+      // normalised by its own sum, so its bf16 rounding moves the merged O by at
+      // most 2^-9 of the largest partial.
+      const bool part_f32 = p.out_fp32 != 0;
       if (nt > 0) {
         const uint32_t last = pseq - 1;
         WAITC(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
         fence_after_sync();
       }
-      // O[row = lane][32 columns] per step, staged in this warp's 2 KB as 64-byte
-      // row segments (32 bf16 or 2 x 16 fp32 columns) and written back whole.
-      for (int c = 0; c < 8; ++c) {
-        const int col = 256 * ch + 32 * c;
-        float v[32];
-        if (nt > 0) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_addr + kTmemO + col, u);
-          tmem_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(u[k]) * inv;
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = 0.f;
-        }
-        if (f32) {
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              *reinterpret_cast<float4*>(epi + swz64(lane, k)) =
-                  make_float4(v[16 * hh + 4 * k], v[16 * hh + 4 * k + 1], v[16 * hh + 4 * k + 2], v[16 * hh + 4 * k + 3]);
-            __syncwarp();
-            epi_rows_out(epi, lane, q4, col + 16 * hh, true, it, half, hrows, p);
-            __syncwarp();
+      // A split item first learns whether it is the last split of its (request,
+      // row group, half) to get here: the others write their partial and count it
+      // done; the last one waits for those counts (it waits only on splits that
+      // are past their MMAs, so it never waits on itself) and merges, its own
+      // share straight from TMEM.
+      int mode = 0;                  // 0: final output, 1: write the partial, 2: merge
+      const int ci = 2 * it.group + half;
+      if (it.slot >= 0 && hrows > 0) {
+        if (warp == 0) {
+          if (lane == 0) {
+            int verdict = 1;
+            if (atomicAdd(&p.counters[ci], 1) == it.S - 1) {
+              verdict = 2;
+              const long long t0 = clock64();
+              while (ld_acquire_gpu(&p.done[ci]) < it.S - 1) {
+                if (bars->abort || clock64() - t0 > p.wait_limit) {
+                  verdict = -1;
+                  break;
+                }
+              }
+              p.counters[ci] = 0;      // nothing else touches this pair of counters in this call
+              p.done[ci] = 0;
+            }
+            bars->merge_last = verdict;
+            mbar_arrive(&bars->mrg_b);
           }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            *reinterpret_cast<uint4*>(epi + swz64(lane, k)) =
-                make_uint4(pack_bf16x2(v[8 * k], v[8 * k + 1]), pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                           pack_bf16x2(v[8 * k + 4], v[8 * k + 5]), pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
           __syncwarp();
-          epi_rows_out(epi, lane, q4, col, false, it, half, hrows, p);
-          __syncwarp();
+        }
+        WAIT(&bars->mrg_b, mrg_b_ph, 44);
+        mrg_b_ph ^= 1;
+        mode = bars->merge_last;
+        if (mode < 0) {
+          fail(bars, p, 47);
+          goto done;
         }
       }
-      if (live && ch == 0) {
-        if (it.slot >= 0) p.part_lse[(int64_t)it.slot * kRows + irow] = lse;
-        else p.lse[row] = lse;
+      if (mode != 2) {
+        // O / l of this thread's row and 256 columns, 32 at a time, to the output
+        // or to this split's partial
+        const bool f32 = mode == 1 ? part_f32 : p.out_fp32 != 0;
+        const int esz = f32 ? 4 : 2;
+        uint8_t* base = mode == 1 ? reinterpret_cast<uint8_t*>(p.part_o) + (int64_t)it.slot * kRows * kDv * esz
+                                  : static_cast<uint8_t*>(p.o) + (it.q_row_base + it.row0) * kDv * esz;
+        for (int c = 0; c < 8; ++c) {
+          const int col = 256 * ch + 32 * c;
+          float v[32];
+          if (nt > 0) {
+            uint32_t u[32];
+            tmem_ld32(tmem + lane_addr + kTmemO + col, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(u[k]) * inv;
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = 0.f;
+          }
+          stage_and_write(v, f32, epi, lane, q4, col, base, (int64_t)kDv * esz, half, hrows);
+        }
+        if (live && ch == 0) {
+          if (mode == 1) p.part_lse[(int64_t)it.slot * kRows + irow] = lse;
+          else p.lse[row] = lse;
+        }
+      } else {
+        // Merge: every split's weight for this row in split order, the own split
+        // taken from TMEM and rounded exactly as its partial would have been.
+        const int B = p.batch;
+        const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
+        const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
+        float M = -INFINITY;
+        for (int s = 0; s < it.S; ++s)
+          M = fmaxf(M, s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow));
+        float tot = 0.f;
+        if (M != -INFINITY)
+          for (int s = 0; s < it.S; ++s) {
+            const float ls = s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
+            tot += ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
+          }
+        const float winv = M == -INFINITY ? 0.f : 1.f / tot;
+        const int oesz = p.out_fp32 ? 4 : 2;
+        uint8_t* obase = static_cast<uint8_t*>(p.o) + (it.q_row_base + it.row0) * kDv * oesz;
+        // Other splits' partial rows: per 16-column step this thread reads 32 bytes
+        // (bf16) or 64 bytes (fp32) of its row from each other split; the first
+        // other split's next step is requested before the current one is combined.
+        const int s_first = it.s == 0 ? 1 : 0;        // the first split that is not this one
+        const bool pipe = !part_f32 && live && s_first < it.S;
+        auto part_bf16 = [&](int s, int col) {
+          return reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.part_o) +
+                                                ((int64_t)(pbase + s * G + it.g) * kRows + irow) * kDv + col);
+        };
+        uint4 nxt0 = make_uint4(0, 0, 0, 0), nxt1 = make_uint4(0, 0, 0, 0);
+        if (pipe) {
+          nxt0 = __ldcg(part_bf16(s_first, 256 * ch));
+          nxt1 = __ldcg(part_bf16(s_first, 256 * ch) + 1);
+        }
+        for (int c = 0; c < 8; ++c) {
+          const int col = 256 * ch + 32 * c;
+          float res[32];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int col16 = col + 16 * hh;
+            const uint4 cur0 = nxt0, cur1 = nxt1;
+            if (pipe && col16 + 16 < 256 * ch + 256) {
+              nxt0 = __ldcg(part_bf16(s_first, col16 + 16));
+              nxt1 = __ldcg(part_bf16(s_first, col16 + 16) + 1);
+            }
+            uint32_t u[16];
+            tmem_ld16(tmem + lane_addr + kTmemO + col16, u);
+            tmem_wait_ld();
+            float acc[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+            for (int s = 0; s < it.S; ++s) {
+              const float ls = s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
+              const float w = (M == -INFINITY || ls == -INFINITY) ? 0.f : ex2((ls - M) * 1.4426950408889634f) * winv;
+              if (s == it.s) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const float o = __uint_as_float(u[k]) * inv;
+                  acc[k] += w * (part_f32 ? o : __bfloat162float(__float2bfloat16_rn(o)));
+                }
+              } else if (live) {
+                if (part_f32) {
+                  const float4* src = reinterpret_cast<const float4*>(
+                      p.part_o + ((int64_t)(pbase + s * G + it.g) * kRows + irow) * kDv + col16);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const float4 q = __ldcg(src + k);
+                    acc[4 * k] += w * q.x;
+                    acc[4 * k + 1] += w * q.y;
+                    acc[4 * k + 2] += w * q.z;
+                    acc[4 * k + 3] += w * q.w;
+                  }
+                } else {
+                  const uint4 q0 = s == s_first ? cur0 : __ldcg(part_bf16(s, col16));
+                  const uint4 q1 = s == s_first ? cur1 : __ldcg(part_bf16(s, col16) + 1);
+                  const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    acc[2 * e] += w * bf16_bits_to_float(wd[e] & 0xFFFFu);
+                    acc[2 * e + 1] += w * bf16_bits_to_float(wd[e] >> 16);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 16; ++k) res[16 * hh + k] = acc[k];
+          }
+          stage_and_write(res, p.out_fp32 != 0, epi, lane, q4, col, obase, (int64_t)kDv * oesz, half, hrows);
+        }
+        if (live && ch == 0) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
       }
       if (nt > 0) {
         fence_before_sync();
         __syncwarp();
         if (lane == 0) arrive_at(&bars->o_free, lead, rank);
       }
-      if (it.slot >= 0 && hrows > 0) {
-        // Fused split merge of this half: the last split of this (request, row
-        // group) to finish combines every split's partial rows in split order.
-        // The row warps first agree (warp 0 counts one arrival per split), then
-        // merge together.
-        __threadfence();
+      if (mode == 1) {
+        // Count this split's partial done: the row warps meet on a CTA barrier,
+        // then one release at GPU scope publishes every store ordered before it.
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->mrg_a);
+        if (lane == 0) mbar_arrive(&bars->mrg_c);
         if (warp == 0) {
-          WAIT(&bars->mrg_a, mrg_a_ph, 43);
-          if (lane == 0) {
-            bars->merge_last = atomicAdd(&p.counters[2 * it.group + half], 1) == it.S - 1;
-            mbar_arrive(&bars->mrg_b);
-          }
-          __syncwarp();
-        }
-        mrg_a_ph ^= 1;
-        WAIT(&bars->mrg_b, mrg_b_ph, 44);
-        mrg_b_ph ^= 1;
-        if (bars->merge_last) {
-          __threadfence();
-          const int B = p.batch;
-          const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
-          const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
-          // pass 1 (column half 0, thread = row): max, normaliser and the weight of every split
-          if (ch == 0) {
-            float M = -INFINITY;
-            if (live)
-              for (int s = 0; s < it.S; ++s)
-                M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow));
-            float tot = 0.f;
-            if (M != -INFINITY)
-              for (int s = 0; s < it.S; ++s) {
-                const float ls = __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
-                const float e = ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
-                wts[s * kHalfRows + r] = e;
-                tot += e;
-              }
-            const float winv = M == -INFINITY ? 0.f : 1.f / tot;
-            for (int s = 0; s < it.S; ++s)
-              wts[s * kHalfRows + r] = M == -INFINITY ? 0.f : wts[s * kHalfRows + r] * winv;
-            if (live) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->mrg_c);
           WAIT(&bars->mrg_c, mrg_c_ph, 45);
-          mrg_c_ph ^= 1;
-          // pass 2: thread t owns float4 column t % 128 of rows of parity t / 128; 8 rows in flight
-          const int c4 = tid & 127, rsub = tid >> 7;
-          for (int rb = 0; rb < hrows; rb += 16) {
-            float4 acc[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s = 0; s < it.S; ++s) {
-              const int slot = pbase + s * G + it.g;
-              float4 ov[8];
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int rr = kHalfRows * half + min(rb + 2 * k + rsub, hrows - 1);
-                ov[k] = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)slot * kRows + rr) * kDv) + c4);
-              }
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const float w = wts[s * kHalfRows + min(rb + 2 * k + rsub, hrows - 1)];
-                acc[k].x += w * ov[k].x;
-                acc[k].y += w * ov[k].y;
-                acc[k].z += w * ov[k].z;
-                acc[k].w += w * ov[k].w;
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int rl = rb + 2 * k + rsub;
-              if (rl >= hrows) break;
-              const int64_t orow = it.q_row_base + it.row0 + kHalfRows * half + rl;
-              if (p.out_fp32) {
-                reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow * kDv)[c4] = acc[k];
-              } else {
-                uint2 u;
-                u.x = pack_bf16x2(acc[k].x, acc[k].y);
-                u.y = pack_bf16x2(acc[k].z, acc[k].w);
-                reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + orow * kDv)[c4] = u;
-              }
-            }
-          }
-          if (tid == 0) p.counters[2 * it.group + half] = 0;
-          // the weights live where the next epilogue stages its rows
+          if (lane == 0) red_release_gpu_add(&p.done[ci], 1);
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bars->mrg_d);
-          WAIT(&bars->mrg_d, mrg_d_ph, 46);
-          mrg_d_ph ^= 1;
         }
+        mrg_c_ph ^= 1;
       }
     }
   }
