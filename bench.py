@@ -758,7 +758,7 @@ def decode_main(args, rank: int, world: int):
     sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
     # The draft block has 32 row groups of 128 KV tiles; 64 workers (two splits
     # each, one item per cluster) measured fastest in a sweep of worker counts.
-    tuned = {"draft_block_bf16": 64} if algo == m.MLA_ALGO_TENSOR else {}
+    tuned = {"draft_block_bf16": 32} if algo == m.MLA_ALGO_TENSOR else {}
     workers = args.workers or tuned.get(args.config) or m.default_workers_for(
         algo, w.batch, w.num_heads, int(w.q_lens().max()), dev_index)
     # Long skewed contexts: every replay brings new lengths, T and indices (the

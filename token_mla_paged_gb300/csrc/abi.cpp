@@ -192,7 +192,6 @@ mla_status mla_decode_fwd(const mla_fwd_args* a, void* stream) {
   }
   dp.ws_hdr = (int32_t*)ws;
   dp.counters = (int32_t*)(ws + wg.counters_off);
-  dp.done = dp.counters + wg.counters_cap / 2;
   dp.part_lse = (float*)(ws + wg.part_lse_off);
   dp.part_o = (float*)(ws + wg.part_o_off);
   return a->algo == MLA_ALGO_TENSOR ? launch_decode_tensor(dp, stream)

@@ -858,49 +858,17 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
         WAITC(&bars->o_ready[last % kPBufs], (last / kPBufs) & 1, 42);
         fence_after_sync();
       }
-      // A split item first learns whether it is the last split of its (request,
-      // row group, half) to get here: the others write their partial and count it
-      // done; the last one waits for those counts (it waits only on splits that
-      // are past their MMAs, so it never waits on itself) and merges, its own
-      // share straight from TMEM.
-      int mode = 0;                  // 0: final output, 1: write the partial, 2: merge
-      const int ci = 2 * it.group + half;
-      if (it.slot >= 0 && hrows > 0) {
-        if (warp == 0) {
-          if (lane == 0) {
-            int verdict = 1;
-            if (atomicAdd(&p.counters[ci], 1) == it.S - 1) {
-              verdict = 2;
-              const long long t0 = clock64();
-              while (ld_acquire_gpu(&p.done[ci]) < it.S - 1) {
-                if (bars->abort || clock64() - t0 > p.wait_limit) {
-                  verdict = -1;
-                  break;
-                }
-              }
-              p.counters[ci] = 0;      // nothing else touches this pair of counters in this call
-              p.done[ci] = 0;
-            }
-            bars->merge_last = verdict;
-            mbar_arrive(&bars->mrg_b);
-          }
-          __syncwarp();
-        }
-        WAIT(&bars->mrg_b, mrg_b_ph, 44);
-        mrg_b_ph ^= 1;
-        mode = bars->merge_last;
-        if (mode < 0) {
-          fail(bars, p, 47);
-          goto done;
-        }
-      }
-      if (mode != 2) {
+      // Split items write their partial (O / l and the LSE of their share of the
+      // KV); the last split of a (request, row group, half) to finish then merges
+      // every split's partial, in split order, into the output.
+      const bool split = it.slot >= 0;
+      {
         // O / l of this thread's row and 256 columns, 32 at a time, to the output
         // or to this split's partial
-        const bool f32 = mode == 1 ? part_f32 : p.out_fp32 != 0;
+        const bool f32 = split ? part_f32 : p.out_fp32 != 0;
         const int esz = f32 ? 4 : 2;
-        uint8_t* base = mode == 1 ? reinterpret_cast<uint8_t*>(p.part_o) + (int64_t)it.slot * kRows * kDv * esz
-                                  : static_cast<uint8_t*>(p.o) + (it.q_row_base + it.row0) * kDv * esz;
+        uint8_t* base = split ? reinterpret_cast<uint8_t*>(p.part_o) + (int64_t)it.slot * kRows * kDv * esz
+                              : static_cast<uint8_t*>(p.o) + (it.q_row_base + it.row0) * kDv * esz;
         for (int c = 0; c < 8; ++c) {
           const int col = 256 * ch + 32 * c;
           float v[32];
@@ -917,114 +885,125 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
           stage_and_write(v, f32, epi, lane, q4, col, base, (int64_t)kDv * esz, half, hrows);
         }
         if (live && ch == 0) {
-          if (mode == 1) p.part_lse[(int64_t)it.slot * kRows + irow] = lse;
+          if (split) p.part_lse[(int64_t)it.slot * kRows + irow] = lse;
           else p.lse[row] = lse;
         }
-      } else {
-        // Merge: every split's weight for this row in split order, the own split
-        // taken from TMEM and rounded exactly as its partial would have been.
-        const int B = p.batch;
-        const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
-        const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
-        float M = -INFINITY;
-        for (int s = 0; s < it.S; ++s)
-          M = fmaxf(M, s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow));
-        float tot = 0.f;
-        if (M != -INFINITY)
-          for (int s = 0; s < it.S; ++s) {
-            const float ls = s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
-            tot += ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
-          }
-        const float winv = M == -INFINITY ? 0.f : 1.f / tot;
-        const int oesz = p.out_fp32 ? 4 : 2;
-        uint8_t* obase = static_cast<uint8_t*>(p.o) + (it.q_row_base + it.row0) * kDv * oesz;
-        // Other splits' partial rows: per 16-column step this thread reads 32 bytes
-        // (bf16) or 64 bytes (fp32) of its row from each other split; the first
-        // other split's next step is requested before the current one is combined.
-        const int s_first = it.s == 0 ? 1 : 0;        // the first split that is not this one
-        const bool pipe = !part_f32 && live && s_first < it.S;
-        auto part_bf16 = [&](int s, int col) {
-          return reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.part_o) +
-                                                ((int64_t)(pbase + s * G + it.g) * kRows + irow) * kDv + col);
-        };
-        uint4 nxt0 = make_uint4(0, 0, 0, 0), nxt1 = make_uint4(0, 0, 0, 0);
-        if (pipe) {
-          nxt0 = __ldcg(part_bf16(s_first, 256 * ch));
-          nxt1 = __ldcg(part_bf16(s_first, 256 * ch) + 1);
-        }
-        for (int c = 0; c < 8; ++c) {
-          const int col = 256 * ch + 32 * c;
-          float res[32];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int col16 = col + 16 * hh;
-            const uint4 cur0 = nxt0, cur1 = nxt1;
-            if (pipe && col16 + 16 < 256 * ch + 256) {
-              nxt0 = __ldcg(part_bf16(s_first, col16 + 16));
-              nxt1 = __ldcg(part_bf16(s_first, col16 + 16) + 1);
-            }
-            uint32_t u[16];
-            tmem_ld16(tmem + lane_addr + kTmemO + col16, u);
-            tmem_wait_ld();
-            float acc[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-            for (int s = 0; s < it.S; ++s) {
-              const float ls = s == it.s ? lse : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
-              const float w = (M == -INFINITY || ls == -INFINITY) ? 0.f : ex2((ls - M) * 1.4426950408889634f) * winv;
-              if (s == it.s) {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const float o = __uint_as_float(u[k]) * inv;
-                  acc[k] += w * (part_f32 ? o : __bfloat162float(__float2bfloat16_rn(o)));
-                }
-              } else if (live) {
-                if (part_f32) {
-                  const float4* src = reinterpret_cast<const float4*>(
-                      p.part_o + ((int64_t)(pbase + s * G + it.g) * kRows + irow) * kDv + col16);
-#pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    const float4 q = __ldcg(src + k);
-                    acc[4 * k] += w * q.x;
-                    acc[4 * k + 1] += w * q.y;
-                    acc[4 * k + 2] += w * q.z;
-                    acc[4 * k + 3] += w * q.w;
-                  }
-                } else {
-                  const uint4 q0 = s == s_first ? cur0 : __ldcg(part_bf16(s, col16));
-                  const uint4 q1 = s == s_first ? cur1 : __ldcg(part_bf16(s, col16) + 1);
-                  const uint32_t wd[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) {
-                    acc[2 * e] += w * bf16_bits_to_float(wd[e] & 0xFFFFu);
-                    acc[2 * e + 1] += w * bf16_bits_to_float(wd[e] >> 16);
-                  }
-                }
-              }
-            }
-#pragma unroll
-            for (int k = 0; k < 16; ++k) res[16 * hh + k] = acc[k];
-          }
-          stage_and_write(res, p.out_fp32 != 0, epi, lane, q4, col, obase, (int64_t)kDv * oesz, half, hrows);
-        }
-        if (live && ch == 0) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
       }
       if (nt > 0) {
         fence_before_sync();
         __syncwarp();
         if (lane == 0) arrive_at(&bars->o_free, lead, rank);
       }
-      if (mode == 1) {
-        // Count this split's partial done: the row warps meet on a CTA barrier,
-        // then one release at GPU scope publishes every store ordered before it.
+      if (split && hrows > 0) {
+        // The row warps meet on a CTA barrier; warp 0 then counts this split in
+        // with an acquire-release add at GPU scope: the partial stores ordered
+        // before the barrier are published with it, and the last split sees every
+        // other split's.
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->mrg_c);
         if (warp == 0) {
           WAIT(&bars->mrg_c, mrg_c_ph, 45);
-          if (lane == 0) red_release_gpu_add(&p.done[ci], 1);
+          if (lane == 0) {
+            bars->merge_last = atom_add_acq_rel_gpu(&p.counters[2 * it.group + half], 1) == it.S - 1;
+            mbar_arrive(&bars->mrg_b);
+          }
           __syncwarp();
         }
         mrg_c_ph ^= 1;
+        WAIT(&bars->mrg_b, mrg_b_ph, 44);
+        mrg_b_ph ^= 1;
+        if (bars->merge_last) {
+          const int B = p.batch;
+          const int G = p.plan[kPlanHeaderInts + B + it.b + 1] - p.plan[kPlanHeaderInts + B + it.b];
+          const int pbase = p.plan[kPlanHeaderInts + 2 * B + 1 + it.b];
+          // pass 1 (column half 0, thread = row): every split's weight for the row
+          float* wts = reinterpret_cast<float*>(smem + kOffEpi0);   // [S][128], 8 KB
+          if (ch == 0) {
+            float M = -INFINITY;
+            if (live)
+              for (int s = 0; s < it.S; ++s)
+                M = fmaxf(M, __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow));
+            float tot = 0.f;
+            for (int s = 0; s < it.S; ++s) {
+              const float ls = M == -INFINITY ? -INFINITY
+                                              : __ldcg(p.part_lse + (int64_t)(pbase + s * G + it.g) * kRows + irow);
+              const float e = ls == -INFINITY ? 0.f : ex2((ls - M) * 1.4426950408889634f);
+              wts[s * kHalfRows + r] = e;
+              tot += e;
+            }
+            const float winv = M == -INFINITY ? 0.f : 1.f / tot;
+            for (int s = 0; s < it.S; ++s) wts[s * kHalfRows + r] *= winv;
+            if (live) p.lse[row] = M == -INFINITY ? -INFINITY : M + logf(tot);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->mrg_c);
+          WAIT(&bars->mrg_c, mrg_c_ph, 46);
+          mrg_c_ph ^= 1;
+          // pass 2: thread t owns 16-byte column unit t % U of rows t / U + kRpp*k
+          // (U units per row: 64 bf16, 128 fp32), four rows in flight per split
+          const int U = part_f32 ? 128 : 64, kRpp = 256 / U;
+          const int cu = tid % U, rp = tid / U;
+          const int ocpu = part_f32 ? 4 : 8;                  // columns per unit
+          for (int rb = rp; rb < hrows; rb += 4 * kRpp) {
+            float acc[4][8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[k][e] = 0.f;
+            for (int s = 0; s < it.S; ++s) {
+              const int64_t slot = pbase + s * G + it.g;
+              uint4 q[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int rl = min(rb + kRpp * k, hrows - 1);
+                const int64_t off = (slot * kRows + kHalfRows * half + rl) * kDv * (part_f32 ? 4 : 2) + 16 * cu;
+                q[k] = __ldcg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(p.part_o) + off));
+              }
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float w = wts[s * kHalfRows + min(rb + kRpp * k, hrows - 1)];
+                const uint32_t wd[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+                if (part_f32) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) acc[k][e] += w * __uint_as_float(wd[e]);
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    acc[k][2 * e] += w * bf16_bits_to_float(wd[e] & 0xFFFFu);
+                    acc[k][2 * e + 1] += w * bf16_bits_to_float(wd[e] >> 16);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int rl = rb + kRpp * k;
+              if (rl >= hrows) break;
+              const int64_t orow = it.q_row_base + it.row0 + kHalfRows * half + rl;
+              const int c0 = ocpu * cu;
+              if (p.out_fp32) {
+                float* dst = static_cast<float*>(p.o) + orow * kDv + c0;
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+                if (ocpu == 8) *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[k][4], acc[k][5], acc[k][6], acc[k][7]);
+              } else {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + orow * kDv + c0;
+                if (ocpu == 8)
+                  *reinterpret_cast<uint4*>(dst) =
+                      make_uint4(pack_bf16x2(acc[k][0], acc[k][1]), pack_bf16x2(acc[k][2], acc[k][3]),
+                                 pack_bf16x2(acc[k][4], acc[k][5]), pack_bf16x2(acc[k][6], acc[k][7]));
+                else
+                  *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[k][0], acc[k][1]),
+                                                              pack_bf16x2(acc[k][2], acc[k][3]));
+              }
+            }
+          }
+          if (tid == 0) p.counters[2 * it.group + half] = 0;   // ready for the next call
+          // the weights live where the next epilogue stages its rows
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->mrg_c);
+          WAIT(&bars->mrg_c, mrg_c_ph, 48);
+          mrg_c_ph ^= 1;
+        }
       }
     }
   }

@@ -50,10 +50,10 @@ inline PlanGeom plan_geom(const mla_plan_params& p) {
 // ---------------------------------------------------------------- workspace layout
 // [0, 256)       header words: 0 error code, 1 error info (both persist until read),
 //                2.. per-call state (queue heads), zeroed at the start of every call
-// counters       int32 [2 * B * g_max]  split arrivals per (b, g, row half), then
-//                int32 [2 * B * g_max]  split partials written, per (b, g, row half)
+// counters       int32 [2 * B * g_max]  split arrivals per (b, g, row half)
 // part_lse       fp32 [items_cap, 256]
-// part_o         fp32 [items_cap, 256, 512]
+// part_o         fp32 or bf16 [items_cap, 256, 512] (the tensor kernel stores bf16
+//                partials when the output is bf16)
 enum WsHeader : int { kWsErrCode = 0, kWsErrInfo = 1, kWsQueue = 2, kWsQueue2 = 3 };
 
 struct WsGeom {
@@ -66,7 +66,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline WsGeom ws_geom(const mla_plan_params& p) {
   PlanGeom pg = plan_geom(p);
   WsGeom w;
-  w.counters_cap = 4 * (int64_t)p.batch * pg.g_max;
+  w.counters_cap = 2 * (int64_t)p.batch * pg.g_max;
   if (w.counters_cap < 1) w.counters_cap = 1;
   w.partial_cap = pg.items_cap;
   w.counters_off = 256;
@@ -101,7 +101,6 @@ struct DecodeParams {
   int32_t test_stall;    // failure-path test: wait on a barrier nothing signals before any work
   int32_t* ws_hdr;
   int32_t* counters;     // split arrivals, [2 * B * g_max]
-  int32_t* done;         // split partials written, [2 * B * g_max]
   float* part_lse;
   float* part_o;
 };

@@ -106,18 +106,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
-// Acquire load of a global word at GPU scope (pairs with a fence + atomic release).
-__device__ __forceinline__ int ld_acquire_gpu(const int* ptr) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-  return v;
-}
-
-// Atomic add with release semantics at GPU scope: every write ordered before it
-// (including other threads' writes ordered by a CTA barrier) is visible to a
-// thread that reads the new value with an acquire load.
-__device__ __forceinline__ void red_release_gpu_add(int* ptr, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+// The release publishes every write ordered before it (including other threads'
+// writes ordered by a CTA barrier); the acquire makes the writes published by
+// earlier adds visible to this thread and to what it orders after.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* ptr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+  return old;
 }
 
 // ------------------------------------------------------------------ proxies
