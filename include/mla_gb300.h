@@ -75,7 +75,7 @@
 extern "C" {
 #endif
 
-#define MLA_ABI_VERSION 5
+#define MLA_ABI_VERSION 6
 #define MLA_D_QK 576             /* latent 512 + RoPE 64 */
 #define MLA_D_V 512
 #define MLA_ROWS_PER_GROUP 256   /* query rows (t,h) of one work item */
@@ -169,7 +169,10 @@ typedef struct {
   void* plan_d;                      /* device plan buffer (STATIC: uploaded host plan;
                                         DYNAMIC: rewritten by this call) */
   size_t plan_bytes;
-  void* workspace_d;                 /* device workspace, >= the size mla_decode_plan_size gives */
+  void* workspace_d;                 /* device workspace, >= the size mla_decode_plan_size gives;
+                                        zero-filled once when allocated (since ABI version 6
+                                        no call clears it: each completed call leaves its
+                                        counters at zero, see mla_get_device_error) */
   size_t ws_bytes;
   /* Index lists that are not a run of positions (since ABI version 3): one index
    * list per layer type -- a sliding window (SWA), a window plus top-k selected
@@ -187,7 +190,10 @@ typedef struct {
  * rather than by inspecting signatures.  3: per-entry positions and the sliding
  * window in mla_fwd_args, HOST plans, mla_cache_write, mla_rope_q_cache;
  * 4: mla_absorb_bmm; 5: work items of 256 query rows over 128-entry tiles (the
- * plan layout changed) and mla_decode_workers. */
+ * plan layout changed) and mla_decode_workers; 6: the workspace is zero-filled
+ * once by its owner instead of being cleared by every call, and the decode and
+ * merge kernels start their set-up while the previous kernel on the stream
+ * finishes. */
 int mla_abi_version(void);
 
 /* Static description of a status code; never NULL. */
@@ -224,7 +230,12 @@ mla_status mla_decode_plan_device(const mla_plan_params* params, const int32_t* 
                                   void* workspace_d, size_t ws_bytes, void* stream);
 
 /* Forward call: O and LSE for every (token, head) of the batch.  DYNAMIC mode
- * first re-plans on the device from the real lengths.  Enqueued on `stream`. */
+ * first re-plans on the device from the real lengths.  Enqueued on `stream`.
+ * The decode kernel is launched with programmatic stream serialisation: its
+ * set-up (barriers, tensor memory) may run while the kernel before it on the
+ * stream finishes, and it reads no input and writes no output before that kernel
+ * has completed.  The workspace must have been zero-filled once; the call uses
+ * no memset and leaves the workspace's counters at zero when it completes. */
 mla_status mla_decode_fwd(const mla_fwd_args* args, void* stream);
 
 /* N-way merge of partial states over disjoint KV subsets:
@@ -233,14 +244,18 @@ mla_status mla_decode_fwd(const mla_fwd_args* args, void* stream);
  *   M = max lse_s;  LSE = M + ln sum exp(lse_s - M);  O = sum exp(lse_s - LSE) O_s.
  * States with lse = -inf add nothing; all -inf gives O = 0, LSE = -inf.  This is
  * the combine step of round-robin context parallelism ("Speculative decode +
- * DCP on gfx1250", Problem).  Enqueued on `stream`. */
+ * DCP on gfx1250", Problem).  Enqueued on `stream`, with programmatic stream
+ * serialisation like mla_decode_fwd: it reads its inputs only after the kernel
+ * before it on the stream has completed. */
 mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const float* lse_parts,
                             int32_t n, int64_t rows, int32_t dv, void* o, int32_t o_dtype,
                             float* lse, void* stream);
 
 /* Read and clear the workspace error word.  Synchronises `stream`; not for use
  * while the stream is being captured.  *code receives an mla_device_error and
- * *info its detail; returns MLA_ERR_DEVICE_FAULT when *code != 0. */
+ * *info its detail; returns MLA_ERR_DEVICE_FAULT when *code != 0.  After a
+ * fault it also zeroes the queue words and split counters the faulted call may
+ * have left set, so the workspace is ready for the next call. */
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info);
 
 /* Dtype of an activation input to mla_cache_write. */
@@ -373,7 +388,9 @@ mla_status mla_absorb_bmm(const mla_absorb_bmm_args* args, void* stream);
  *     MLA_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
  *   - Allocates nothing.  The first call on a device looks up that device's
  *     copy of the array (cudaGetSymbolAddress); make it before any stream
- *     capture.  The array stays resident while the library is loaded.
+ *     capture.  Host threads whose first calls on a device coincide each look
+ *     it up and store the same address (an atomic store), so they may race
+ *     harmlessly.  The array stays resident while the library is loaded.
  *   - All calls share the array: calls that overlap on the GPU race on it.
  *     Each call clears the state that must start at zero.
  *   - Device-side faults are recorded in the array's error word, which this ABI

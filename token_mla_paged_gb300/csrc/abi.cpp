@@ -45,6 +45,101 @@ int device_sm_count(int dev) {
   return sms[dev];
 }
 
+mla_status decode_fwd_impl(const mla_fwd_args* a, void* stream, bool clear_state) {
+  if (!a || !params_valid(a->params)) return MLA_ERR_INVALID_ARG;
+  const mla_plan_params& p = *a->params;
+  if (a->kv_dtype != MLA_KV_BF16 && a->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (a->out_dtype != MLA_OUT_BF16 && a->out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
+  if (a->algo != MLA_ALGO_TENSOR && a->algo != MLA_ALGO_CUDA_CORE) return MLA_ERR_INVALID_ARG;
+  if (a->causal != 0 && a->causal != 1) return MLA_ERR_INVALID_ARG;
+  if (!(std::isfinite(a->softmax_scale) && a->softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
+  if (a->kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(a->kv_scale) && a->kv_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (a->pos_stride < 1) return MLA_ERR_INVALID_ARG;
+  if (a->window < 0 || (a->kv_pos && !aligned(a->kv_pos, 4))) return MLA_ERR_INVALID_ARG;
+  if (a->num_slots <= 0 || a->num_slots > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (p.batch > 0) {
+    if (!a->q || !a->kv_pool || !a->kv_indptr || !a->kv_indices || !a->qo_indptr || !a->o ||
+        !a->lse)
+      return MLA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->kv_pool, 16) || !aligned(a->o, 16) ||
+        !aligned(a->lse, 4) || !aligned(a->kv_indptr, 4) || !aligned(a->kv_indices, 4) ||
+        !aligned(a->qo_indptr, 4))
+      return MLA_ERR_INVALID_ARG;
+  }
+  if (!a->plan_d || !a->workspace_d) return MLA_ERR_INVALID_ARG;
+  if (!aligned(a->plan_d, 16) || !aligned(a->workspace_d, 256)) return MLA_ERR_INVALID_ARG;
+  const PlanGeom pg = plan_geom(p);
+  if (pg.items_cap > kCostClamp) return MLA_ERR_UNSUPPORTED;
+  if (a->plan_bytes < sizeof(int32_t) * (size_t)pg.total_ints) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  const WsGeom wg = ws_geom(p);
+  if (a->ws_bytes < wg.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (a->algo == MLA_ALGO_TENSOR && !tensor_kernel_available()) return MLA_ERR_UNSUPPORTED;
+  if (p.mode == MLA_PLAN_DYNAMIC && (p.batch > 4096 || pg.items_cap > 8192))
+    return MLA_ERR_UNSUPPORTED;
+
+  char* ws = (char*)a->workspace_d;
+  cudaStream_t st = (cudaStream_t)stream;
+  // The queue words and split counters are left at zero by every completed call;
+  // a caller whose workspace is not kept between calls asks for them to be cleared.
+  if (clear_state &&
+      cudaMemsetAsync(ws + 8, 0, wg.counters_off - 8 + 4 * (size_t)wg.counters_cap, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (p.batch == 0) return MLA_OK;
+  if (p.mode == MLA_PLAN_DYNAMIC) {
+    mla_status s = launch_plan_device(p, a->kv_indptr, a->qo_indptr, (int32_t*)a->plan_d,
+                                      (int32_t*)ws, stream);
+    if (s != MLA_OK) return s;
+  }
+
+  DecodeParams dp;
+  std::memset(&dp, 0, sizeof(dp));
+  dp.q = a->q;
+  dp.kv = a->kv_pool;
+  dp.num_slots = a->num_slots;
+  dp.kv_fp8 = a->kv_dtype == MLA_KV_FP8_E4M3;
+  dp.out_fp32 = a->out_dtype == MLA_OUT_FP32;
+  dp.kv_indptr = a->kv_indptr;
+  dp.kv_indices = a->kv_indices;
+  dp.qo_indptr = a->qo_indptr;
+  dp.pos_base_per_req = a->pos_base_per_req;
+  dp.g_kv_indptr = a->g_kv_indptr;
+  dp.causal = a->causal;
+  dp.pos_base = a->pos_base;
+  dp.pos_stride = a->pos_stride;
+  dp.kv_pos = a->kv_pos;
+  dp.window = a->window;
+  dp.batch = p.batch;
+  dp.num_heads = p.num_heads;
+  dp.max_q_len = p.max_q_len;
+  dp.num_workers = p.num_workers;
+  dp.mode = p.mode;
+  dp.items_cap = pg.items_cap;
+  const float kappa = dp.kv_fp8 ? a->kv_scale : 1.0f;
+  dp.scale_log2 = (float)((double)a->softmax_scale * (double)kappa * 1.4426950408889634);
+  dp.out_scale = kappa;
+  dp.o = a->o;
+  dp.lse = a->lse;
+  dp.plan = (const int32_t*)a->plan_d;
+  dp.wait_limit = 2000000000LL;   // about a second at GB300 clocks
+  // Failure-path test hook (tests only): MLA_TEST_STALL_CYCLES=<n> makes the
+  // tensor kernel wait on a barrier nothing signals, with a limit of n cycles.
+  if (const char* e = std::getenv("MLA_TEST_STALL_CYCLES")) {
+    const long long n = std::atoll(e);
+    if (n > 0) {
+      dp.test_stall = 1;
+      dp.wait_limit = n;
+    }
+  }
+  dp.ws_hdr = (int32_t*)ws;
+  dp.counters = (int32_t*)(ws + wg.counters_off);
+  dp.counters_words = (int32_t)wg.counters_cap;
+  dp.part_lse = (float*)(ws + wg.part_lse_off);
+  dp.part_o = (float*)(ws + wg.part_o_off);
+  return a->algo == MLA_ALGO_TENSOR ? launch_decode_tensor(dp, stream)
+                                    : launch_decode_cuda_core(dp, stream);
+}
+
 }  // namespace mla
 
 extern "C" {
@@ -106,96 +201,7 @@ mla_status mla_decode_plan_device(const mla_plan_params* params, const int32_t* 
 }
 
 mla_status mla_decode_fwd(const mla_fwd_args* a, void* stream) {
-  if (!a || !params_valid(a->params)) return MLA_ERR_INVALID_ARG;
-  const mla_plan_params& p = *a->params;
-  if (a->kv_dtype != MLA_KV_BF16 && a->kv_dtype != MLA_KV_FP8_E4M3) return MLA_ERR_INVALID_ARG;
-  if (a->out_dtype != MLA_OUT_BF16 && a->out_dtype != MLA_OUT_FP32) return MLA_ERR_INVALID_ARG;
-  if (a->algo != MLA_ALGO_TENSOR && a->algo != MLA_ALGO_CUDA_CORE) return MLA_ERR_INVALID_ARG;
-  if (a->causal != 0 && a->causal != 1) return MLA_ERR_INVALID_ARG;
-  if (!(std::isfinite(a->softmax_scale) && a->softmax_scale > 0.f)) return MLA_ERR_INVALID_ARG;
-  if (a->kv_dtype == MLA_KV_FP8_E4M3 && !(std::isfinite(a->kv_scale) && a->kv_scale > 0.f))
-    return MLA_ERR_INVALID_ARG;
-  if (a->pos_stride < 1) return MLA_ERR_INVALID_ARG;
-  if (a->window < 0 || (a->kv_pos && !aligned(a->kv_pos, 4))) return MLA_ERR_INVALID_ARG;
-  if (a->num_slots <= 0 || a->num_slots > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
-  if (p.batch > 0) {
-    if (!a->q || !a->kv_pool || !a->kv_indptr || !a->kv_indices || !a->qo_indptr || !a->o ||
-        !a->lse)
-      return MLA_ERR_INVALID_ARG;
-    if (!aligned(a->q, 16) || !aligned(a->kv_pool, 16) || !aligned(a->o, 16) ||
-        !aligned(a->lse, 4) || !aligned(a->kv_indptr, 4) || !aligned(a->kv_indices, 4) ||
-        !aligned(a->qo_indptr, 4))
-      return MLA_ERR_INVALID_ARG;
-  }
-  if (!a->plan_d || !a->workspace_d) return MLA_ERR_INVALID_ARG;
-  if (!aligned(a->plan_d, 16) || !aligned(a->workspace_d, 256)) return MLA_ERR_INVALID_ARG;
-  const PlanGeom pg = plan_geom(p);
-  if (pg.items_cap > kCostClamp) return MLA_ERR_UNSUPPORTED;
-  if (a->plan_bytes < sizeof(int32_t) * (size_t)pg.total_ints) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  const WsGeom wg = ws_geom(p);
-  if (a->ws_bytes < wg.total) return MLA_ERR_WORKSPACE_TOO_SMALL;
-  if (a->algo == MLA_ALGO_TENSOR && !tensor_kernel_available()) return MLA_ERR_UNSUPPORTED;
-  if (p.mode == MLA_PLAN_DYNAMIC && (p.batch > 4096 || pg.items_cap > 8192))
-    return MLA_ERR_UNSUPPORTED;
-
-  char* ws = (char*)a->workspace_d;
-  cudaStream_t st = (cudaStream_t)stream;
-  // Per-call state: queue heads (header words 2..63) and the split-merge counters.
-  if (cudaMemsetAsync(ws + 8, 0, wg.counters_off - 8 + 4 * (size_t)wg.counters_cap, st) !=
-      cudaSuccess)
-    return MLA_ERR_CUDA;
-  if (p.batch == 0) return MLA_OK;
-  if (p.mode == MLA_PLAN_DYNAMIC) {
-    mla_status s = launch_plan_device(p, a->kv_indptr, a->qo_indptr, (int32_t*)a->plan_d,
-                                      (int32_t*)ws, stream);
-    if (s != MLA_OK) return s;
-  }
-
-  DecodeParams dp;
-  std::memset(&dp, 0, sizeof(dp));
-  dp.q = a->q;
-  dp.kv = a->kv_pool;
-  dp.num_slots = a->num_slots;
-  dp.kv_fp8 = a->kv_dtype == MLA_KV_FP8_E4M3;
-  dp.out_fp32 = a->out_dtype == MLA_OUT_FP32;
-  dp.kv_indptr = a->kv_indptr;
-  dp.kv_indices = a->kv_indices;
-  dp.qo_indptr = a->qo_indptr;
-  dp.pos_base_per_req = a->pos_base_per_req;
-  dp.g_kv_indptr = a->g_kv_indptr;
-  dp.causal = a->causal;
-  dp.pos_base = a->pos_base;
-  dp.pos_stride = a->pos_stride;
-  dp.kv_pos = a->kv_pos;
-  dp.window = a->window;
-  dp.batch = p.batch;
-  dp.num_heads = p.num_heads;
-  dp.max_q_len = p.max_q_len;
-  dp.num_workers = p.num_workers;
-  dp.mode = p.mode;
-  dp.items_cap = pg.items_cap;
-  const float kappa = dp.kv_fp8 ? a->kv_scale : 1.0f;
-  dp.scale_log2 = (float)((double)a->softmax_scale * (double)kappa * 1.4426950408889634);
-  dp.out_scale = kappa;
-  dp.o = a->o;
-  dp.lse = a->lse;
-  dp.plan = (const int32_t*)a->plan_d;
-  dp.wait_limit = 2000000000LL;   // about a second at GB300 clocks
-  // Failure-path test hook (tests only): MLA_TEST_STALL_CYCLES=<n> makes the
-  // tensor kernel wait on a barrier nothing signals, with a limit of n cycles.
-  if (const char* e = std::getenv("MLA_TEST_STALL_CYCLES")) {
-    const long long n = std::atoll(e);
-    if (n > 0) {
-      dp.test_stall = 1;
-      dp.wait_limit = n;
-    }
-  }
-  dp.ws_hdr = (int32_t*)ws;
-  dp.counters = (int32_t*)(ws + wg.counters_off);
-  dp.part_lse = (float*)(ws + wg.part_lse_off);
-  dp.part_o = (float*)(ws + wg.part_o_off);
-  return a->algo == MLA_ALGO_TENSOR ? launch_decode_tensor(dp, stream)
-                                    : launch_decode_cuda_core(dp, stream);
+  return decode_fwd_impl(a, stream, false);
 }
 
 mla_status mla_merge_states(const void* o_parts, int32_t o_parts_dtype, const float* lse_parts,
@@ -275,12 +281,16 @@ mla_status mla_absorb_bmm(const mla_absorb_bmm_args* a, void* stream) {
 
 mla_status mla_get_device_error(void* workspace_d, void* stream, int32_t* code, int32_t* info) {
   if (!workspace_d || !code) return MLA_ERR_INVALID_ARG;
-  int32_t h[2] = {0, 0};
+  int32_t h[kWsCounterWords + 1] = {0};
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemcpyAsync(h, workspace_d, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return MLA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
-  if (cudaMemsetAsync(workspace_d, 0, sizeof(h), st) != cudaSuccess) return MLA_ERR_CUDA;
+  // A call that stopped on a fault may have left the queue words or split
+  // counters (header word 4 holds how many the last call used) non-zero.
+  const size_t clear = h[0] == 0 ? 2 * sizeof(int32_t)
+                                 : 256 + sizeof(int32_t) * (size_t)(h[kWsCounterWords] > 0 ? h[kWsCounterWords] : 0);
+  if (cudaMemsetAsync(workspace_d, 0, clear, st) != cudaSuccess) return MLA_ERR_CUDA;
   if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
   *code = h[0];
   if (info) *info = h[1];

@@ -66,6 +66,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_cuda_core_kernel(Decod
   __shared__ int s_valid[kTile];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  if (blockIdx.x == 0 && tid == 0) p.ws_hdr[kWsCounterWords] = p.counters_words;
   if (!plan_header_ok(p.plan, p)) {
     if (blockIdx.x == 0 && tid == 0) record_error(p.ws_hdr, MLA_DEV_PLAN_MISMATCH, 0);
     return;
@@ -227,6 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_cuda_core_kernel(Decod
     }
     if (it.slot >= 0) arrive_and_merge(p, it, &s_flag);
   }
+  // The last worker out rewinds the queue for the next call: every worker's final
+  // fetch is ordered before its count, and the count before the reset.
+  if (tid == 0) {
+    __threadfence();
+    if (atomicAdd(&p.ws_hdr[kWsQueueDone], 1) == (int)gridDim.x - 1) {
+      __threadfence();
+      p.ws_hdr[kWsQueue] = 0;
+      p.ws_hdr[kWsQueueDone] = 0;
+    }
+  }
 }
 
 }  // namespace
@@ -243,8 +256,10 @@ mla_status launch_decode_cuda_core(const DecodeParams& dp, void* stream) {
       return MLA_ERR_CUDA;
     attr_done[dev] = true;
   }
-  mla_decode_cuda_core_kernel<<<num_sms, kThreads, smem, (cudaStream_t)stream>>>(dp);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_overlapped(mla_decode_cuda_core_kernel, dim3(num_sms), dim3(kThreads), smem, (cudaStream_t)stream,
+                           dp) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace mla

@@ -286,14 +286,10 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
   const uint32_t lead = rank & ~1u;               // even rank of this CTA's pair
   const uint32_t out_peer = rank ^ 2u;            // same half on the other side
 
-  if (!plan_header_ok(p.plan, p)) {
-    if (blockIdx.x == 0 && tid == 0) record_error(p.ws_hdr, MLA_DEV_PLAN_MISMATCH, 0);
-    return;   // every CTA of every cluster leaves before touching another
-  }
-  const int n_items = p.plan[kHNItems];
   const int cluster = (int)cluster_id_x(), n_clusters = (int)num_clusters_x();
-  if (score_cta && tid == 0) prefetch_q_rows(p, item_of(0, cluster, n_clusters), n_items, half);
 
+  // Set-up first: it reads nothing an earlier kernel writes, so it overlaps the
+  // end of that kernel (the device planner, in the re-planning mode).
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->full[s], kFp8 ? kConvWarps : 1);
@@ -335,6 +331,15 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
   const uint32_t tmem = bars->tmem_base;
   uint8_t* tiles = smem + kOffTiles;
   uint8_t* pbufs = smem + kOffPBuf;
+  grid_dependency_wait();
+  allow_dependent_launch();
+  // A plan that does not match the call runs no item: every CTA goes straight to
+  // the teardown.
+  const bool plan_ok = plan_header_ok(p.plan, p);
+  if (!plan_ok && blockIdx.x == 0 && tid == 0) record_error(p.ws_hdr, MLA_DEV_PLAN_MISMATCH, 0);
+  const int n_items = plan_ok ? p.plan[kHNItems] : 0;
+  if (blockIdx.x == 0 && tid == 0) p.ws_hdr[kWsCounterWords] = p.counters_words;
+  if (score_cta && tid == 0) prefetch_q_rows(p, item_of(0, cluster, n_clusters), n_items, half);
   // Failure-path test: every warp waits on a barrier nothing signals, before any
   // copy or MMA is issued, so the bounded wait runs out with nothing in flight
   // and the kernel records the timeout and tears down.
@@ -1090,9 +1095,10 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
     kp.scale_log2 = dp.scale_log2 * 5.192296858534828e33f;
     kp.out_scale = dp.out_scale * 5.192296858534828e33f;
   }
-  mla_decode_tensor_kernel<kFp8>
-      <<<4 * clusters, kThreads, kSmemBytes + kSmemAlign, (cudaStream_t)stream>>>(tk, tv, kp);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_overlapped(mla_decode_tensor_kernel<kFp8>, dim3(4 * clusters), dim3(kThreads),
+                           kSmemBytes + kSmemAlign, (cudaStream_t)stream, tk, tv, kp) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace

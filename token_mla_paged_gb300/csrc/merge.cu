@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256)
 mla_merge_states_kernel(const void* __restrict__ o_parts, int parts_fp32,
                         const float* __restrict__ lse_parts, int n, int64_t rows, int dv,
                         void* __restrict__ o, int o_fp32, float* __restrict__ lse) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows;
@@ -92,6 +94,8 @@ template <bool kPartsF32, bool kOutF32, int kMaxN>
 __global__ void __launch_bounds__(256)
 mla_merge_states_vec_kernel(const void* __restrict__ o_parts, const float* __restrict__ lse_parts, int n,
                             int64_t rows, int dv, void* __restrict__ o, float* __restrict__ lse) {
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int lane = threadIdx.x & 31;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < rows; r += warps_total) {
@@ -187,11 +191,15 @@ mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const floa
       kern = pick(mla_merge_states_vec_kernel<false, true, 8>, mla_merge_states_vec_kernel<false, true, 16>);
     else
       kern = pick(mla_merge_states_vec_kernel<false, false, 8>, mla_merge_states_vec_kernel<false, false, 16>);
-    kern<<<grid, 256, 0, st>>>(o_parts, lse_parts, n, rows, dv, o, lse);
-  } else {
-    mla_merge_states_kernel<<<grid, 256, 0, st>>>(o_parts, o_parts_fp32, lse_parts, n, rows, dv, o, o_fp32, lse);
+    return launch_overlapped(kern, dim3(grid), dim3(256), 0, st, o_parts, lse_parts, n, rows, dv, o, lse) ==
+                   cudaSuccess
+               ? MLA_OK
+               : MLA_ERR_CUDA;
   }
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_overlapped(mla_merge_states_kernel, dim3(grid), dim3(256), 0, st, o_parts, o_parts_fp32, lse_parts,
+                           n, rows, dv, o, o_fp32, lse) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace mla

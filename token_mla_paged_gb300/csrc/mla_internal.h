@@ -2,6 +2,8 @@
 // the MLA paged-decode library.  Nothing here is part of the public ABI.
 #pragma once
 
+#include <utility>
+
 #include <stddef.h>
 #include <stdint.h>
 
@@ -49,12 +51,18 @@ inline PlanGeom plan_geom(const mla_plan_params& p) {
 
 // ---------------------------------------------------------------- workspace layout
 // [0, 256)       header words: 0 error code, 1 error info (both persist until read),
-//                2.. per-call state (queue heads), zeroed at the start of every call
+//                2 queue head, 3 workers finished (CUDA-core kernel), 4 counter words
+//                of the last call (written by the decode kernels)
 // counters       int32 [2 * B * g_max]  split arrivals per (b, g, row half)
+// The queue words and the counters start at zero (the workspace is zero-filled
+// once, when it is allocated) and every call that completes leaves them at zero
+// again: the last split of a group and the last worker to finish reset what they
+// used.  A call that stopped on a device fault may leave them dirty, so reading the
+// fault (mla_get_device_error) clears them.
 // part_lse       fp32 [items_cap, 256]
 // part_o         fp32 or bf16 [items_cap, 256, 512] (the tensor kernel stores bf16
 //                partials when the output is bf16)
-enum WsHeader : int { kWsErrCode = 0, kWsErrInfo = 1, kWsQueue = 2, kWsQueue2 = 3 };
+enum WsHeader : int { kWsErrCode = 0, kWsErrInfo = 1, kWsQueue = 2, kWsQueueDone = 3, kWsCounterWords = 4 };
 
 struct WsGeom {
   size_t counters_off, part_lse_off, part_o_off, total;
@@ -101,6 +109,7 @@ struct DecodeParams {
   int32_t test_stall;    // failure-path test: wait on a barrier nothing signals before any work
   int32_t* ws_hdr;
   int32_t* counters;     // split arrivals, [2 * B * g_max]
+  int32_t counters_words;
   float* part_lse;
   float* part_o;
 };
@@ -114,6 +123,9 @@ mla_status plan_build_host(const mla_plan_params& p, const int32_t* kv_indptr,
 mla_status launch_plan_device(const mla_plan_params& p, const int32_t* kv_indptr,
                               const int32_t* qo_indptr, int32_t* plan, int32_t* ws_hdr,
                               void* stream);
+// mla_decode_fwd; clear_state zeroes the queue words and split counters first
+// (for a workspace that is not kept between calls).
+mla_status decode_fwd_impl(const mla_fwd_args* a, void* stream, bool clear_state);
 mla_status launch_decode_cuda_core(const DecodeParams& dp, void* stream);
 mla_status launch_decode_tensor(const DecodeParams& dp, void* stream);
 mla_status launch_merge_states(const void* o_parts, int o_parts_fp32, const float* lse_parts,
@@ -133,5 +145,30 @@ int tensor_kernel_workers();   // clusters of the tensor kernel resident at once
 constexpr int kMaxDevices = 64;
 int current_device_slot();
 int device_sm_count(int dev);   // 0 on error
+
+#ifdef __CUDACC__
+// Launch with programmatic stream serialisation: the kernel may start while the
+// kernel before it on the stream is still running, once every block of that
+// kernel has signalled (griddepcontrol.launch_dependents) or exited.  The kernel
+// must execute griddepcontrol.wait before it reads anything an earlier kernel
+// wrote; the wait returns once the earlier kernels have completed and their
+// writes are visible.  After a copy, a memset or a host node the launch is
+// ordered as usual.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
 
 }  // namespace mla

@@ -11,11 +11,15 @@
 // is loaded on a device: every GPU that loads the library holds it until the
 // process exits.  Its device address is looked up once per device, on the first
 // call made with that device current (cudaGetSymbolAddress); make that first
-// call before any stream capture.  All calls share the array and it keeps the
+// call before any stream capture.  The address is kept in an atomic slot: host
+// threads whose first calls coincide each look it up and store the same value.
+// All calls share the array and it keeps the
 // last call's contents, so two calls that overlap on the GPU (different streams
 // without ordering) race on it.  What must start at zero is cleared by every
 // call (queue heads and split-merge counters); the plan is rebuilt on the device
 // by every call, which is why only the re-planning (DYNAMIC) mode is accepted.
+#include <atomic>
+
 #include <cuda_runtime.h>
 
 #include "mla_internal.h"
@@ -27,7 +31,7 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+std::atomic<void*> g_scratch_addr[kMaxDevices];   // zero-initialised (static storage)
 
 }  // namespace
 }  // namespace mla
@@ -46,17 +50,17 @@ extern "C" mla_status mla_decode_fwd_noalloc(const mla_fwd_args* args, void* str
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
-  if (g_scratch_addr[dev] == nullptr) {
+  void* base = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (base == nullptr) {
     // Host code must not use the array's name as an address: ask the runtime for
     // the device address of this device's copy.
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return MLA_ERR_CUDA;
-    g_scratch_addr[dev] = ptr;
+    if (cudaGetSymbolAddress(&base, g_noalloc_scratch) != cudaSuccess || base == nullptr) return MLA_ERR_CUDA;
+    g_scratch_addr[dev].store(base, std::memory_order_release);
   }
   mla_fwd_args a = *args;
-  a.plan_d = g_scratch_addr[dev];
+  a.plan_d = base;
   a.plan_bytes = plan_bytes;
-  a.workspace_d = static_cast<unsigned char*>(g_scratch_addr[dev]) + plan_span;
+  a.workspace_d = static_cast<unsigned char*>(base) + plan_span;
   a.ws_bytes = kNoAllocScratchBytes - plan_span;
-  return mla_decode_fwd(&a, stream);
+  return decode_fwd_impl(&a, stream, true);
 }

@@ -70,6 +70,7 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
   __shared__ int warp_tmp[33];
   __shared__ unsigned long long s_total;
   const int tid = threadIdx.x;
+  allow_dependent_launch();   // the decode kernel's set-up may overlap this plan
 
   if (tid == 0) s_total = 0ull;
   __syncthreads();
