@@ -189,6 +189,10 @@ __global__ void __launch_bounds__(threads_for(kFp8), 1)
   fence_after_sync();
   const uint32_t tmem = bars->tmem_slot;
   const uint32_t sbase = smem_u32(smem);
+  // The set-up above overlaps the end of the previous kernel on the stream; the
+  // activations it may have written are read only after this wait.
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -443,8 +447,10 @@ mla_status launch_absorb_bmm(const mla_absorb_bmm_args& a, void* stream) {
       return MLA_ERR_CUDA;
     smem_set[dev][fp8] = smem;
   }
-  kern<<<grid, threads_for(fp8), smem, (cudaStream_t)stream>>>(tx, tw, p);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_overlapped(kern, dim3(grid), dim3(threads_for(fp8)), smem, (cudaStream_t)stream, tx, tw, p) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace mla

@@ -9,12 +9,6 @@
 
 namespace mla {
 
-// Programmatic dependent launch: wait until the kernels this one may overlap have
-// completed and their writes are visible (a no-op when it was launched in order),
-// and let the next kernel on the stream start launching.
-__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-
 __device__ __forceinline__ void record_error(int32_t* hdr, int code, int info) {
   if (atomicCAS(&hdr[kWsErrCode], 0, code) == 0) atomicExch(&hdr[kWsErrInfo], info);
 }

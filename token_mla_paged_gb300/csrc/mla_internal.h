@@ -147,6 +147,12 @@ int current_device_slot();
 int device_sm_count(int dev);   // 0 on error
 
 #ifdef __CUDACC__
+// Programmatic dependent launch, device side: wait until the kernels this one may
+// overlap have completed and their writes are visible (a no-op when it was
+// launched in order), and let the next kernel on the stream start launching.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // Launch with programmatic stream serialisation: the kernel may start while the
 // kernel before it on the stream is still running, once every block of that
 // kernel has signalled (griddepcontrol.launch_dependents) or exited.  The kernel
