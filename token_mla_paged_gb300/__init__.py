@@ -314,6 +314,7 @@ def mla_get_device_error(workspace_d, stream=None) -> Tuple[int, int]:
 
 
 from .runner import DecodeRunner, default_workers_for  # noqa: E402  (plumbing: buffers + calls, no compute)
+from .cp import gather_states, cp_merge  # noqa: E402  (plumbing: the CP exchange, then the merge kernel)
 
 
 def mla_absorb_bmm(x, w, out, w_scale: float = 1.0, status=None, stream=None) -> None:
