@@ -844,9 +844,12 @@ def decode_main(args, rank: int, world: int):
     ms_med = statistics.median(step_ms)
     ms_max = slowest_rank_ms(ms_med, world, device="cuda")
     rate_job = rate_med * world * ms_med / ms_max      # weak scaling at the slowest rank's time
-    dec_tf = [flops[r % len(flops)] / (t * 1e-3) for t, r in zip(dec_ms, which)]
     dec_med_ms = statistics.median(dec_ms)
-    k_med = sorted(range(len(dec_tf)), key=lambda k: dec_tf[k])[len(dec_tf) // 2]
+    # The roofline launch: the median-rate step over the replays of draw 0, the draw
+    # the committed ncu capture profiled (one launch of it after the warm-up), so
+    # `achieved` and `traffic` describe the same launch; one draw only elsewhere.
+    draw0 = [k for k in range(args.steps) if which[k] == 0]
+    k_med = sorted(draw0, key=lambda k: dec_ms[k])[len(draw0) // 2]
     r_med = which[k_med]
 
     # End to end through the public API: host (pinned) q + index lists in, O + LSE out.
