@@ -755,9 +755,8 @@ def decode_main(args, rank: int, world: int):
     w, extra = build_workload(args.config)
     shards = extra["shards"]
     algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
-    sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
-    # The draft block has 32 row groups of 128 KV tiles; 64 workers (two splits
-    # each, one item per cluster) measured fastest in a sweep of worker counts.
+    # The draft block has 16 row groups of 256 rows over 64 KV tiles; 32 workers (two
+    # splits each, one item per cluster) measured faster than 64 (two items a cluster).
     tuned = {"draft_block_bf16": 32} if algo == m.MLA_ALGO_TENSOR else {}
     workers = args.workers or tuned.get(args.config) or m.default_workers_for(
         algo, w.batch, w.num_heads, int(w.q_lens().max()), dev_index)
