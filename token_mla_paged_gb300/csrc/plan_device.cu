@@ -4,7 +4,9 @@
 // plans; HCA on aiter's persistent V4-NM kernel", Summary part 2: the kernel
 // plans the split from the real per-row KV lengths every call).
 //
-// One block of 1024 threads.  The output is bit-identical to the host planner
+// One block of 64-1024 threads (sized to the batch and the item count: every
+// block-wide barrier costs in proportion to the warps it waits for, and small
+// problems are barrier-bound).  The output is bit-identical to the host planner
 // on the same lengths: integer arithmetic only, and the cost-descending stable
 // order is obtained by sorting unique keys ((65535 - cost) << 16 | enumeration
 // index) with a bitonic network in shared memory.
@@ -15,12 +17,13 @@
 namespace mla {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreadsMax = 1024;
 
 // Exclusive scan of v[0..n) in place (int32), block-wide; returns the total.
 __device__ int block_excl_scan(int* v, int n, int* warp_tmp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int per = (n + nthreads - 1) / nthreads;
   const int lo = min(n, tid * per), hi = min(n, lo + per);
   int local = 0;
   for (int i = lo; i < hi; ++i) local += v[i];
@@ -33,7 +36,7 @@ __device__ int block_excl_scan(int* v, int n, int* warp_tmp) {
   if (lane == 31) warp_tmp[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_tmp[lane];
+    int w = lane < nwarps ? warp_tmp[lane] : 0;
     int wi = w;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -55,7 +58,7 @@ __device__ int block_excl_scan(int* v, int n, int* warp_tmp) {
   return total;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1)
+__global__ void __launch_bounds__(kPlanThreadsMax, 1)
 mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
                 const int32_t* __restrict__ kv_indptr, const int32_t* __restrict__ qo_indptr,
                 int32_t* __restrict__ plan, int32_t* __restrict__ ws_hdr) {
@@ -69,13 +72,16 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
   uint32_t* keys = reinterpret_cast<uint32_t*>(sPb + (B + 1));   // [p2cap]
   __shared__ int warp_tmp[33];
   __shared__ unsigned long long s_total;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  // The lengths may come from the kernel before this one, and the plan buffer may
+  // still be read by the previous call's decode: wait for both before touching them.
+  grid_dependency_wait();
   allow_dependent_launch();   // the decode kernel's set-up may overlap this plan
 
   if (tid == 0) s_total = 0ull;
   __syncthreads();
   unsigned long long local_total = 0;
-  for (int b = tid; b < B; b += kPlanThreads) {
+  for (int b = tid; b < B; b += nthreads) {
     int T = qo_indptr[b + 1] - qo_indptr[b];
     int L = kv_indptr[b + 1] - kv_indptr[b];
     if (T < 0 || L < 0) {
@@ -98,7 +104,7 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
   const int64_t total = (int64_t)s_total;
   int64_t target = (total + W - 1) / W;
   if (target < kMinTiles) target = kMinTiles;
-  for (int b = tid; b < B; b += kPlanThreads) {
+  for (int b = tid; b < B; b += nthreads) {
     int64_t S = ((int64_t)sN[b] + target - 1) / target;
     S = S < 1 ? 1 : (S > kMaxSplits ? kMaxSplits : S);
     sS[b] = (int)S;
@@ -142,7 +148,7 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
     plan[kHItemsCap] = items_cap;
     plan[kHReserved] = 0;
   }
-  for (int b = tid; b <= B; b += kPlanThreads) {
+  for (int b = tid; b <= B; b += nthreads) {
     if (b < B) {
       plan[off_S + b] = sS[b];
       plan[off_p + b] = sS[b] > 1 ? sPb[b] : -1;
@@ -153,9 +159,9 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
   // Sort keys: cost descending, then enumeration order.
   int p2 = 1;
   while (p2 < n_items) p2 <<= 1;
-  for (int k = tid; k < p2; k += kPlanThreads) keys[k] = 0xFFFFFFFFu;
+  for (int k = tid; k < p2; k += nthreads) keys[k] = 0xFFFFFFFFu;
   __syncthreads();
-  for (int b = tid; b < B; b += kPlanThreads) {
+  for (int b = tid; b < B; b += nthreads) {
     const int S = sS[b], G = sG[b], N = sN[b];
     for (int s = 0; s < S; ++s) {
       const int64_t t0 = (int64_t)s * N / S, t1 = (int64_t)(s + 1) * N / S;
@@ -169,7 +175,7 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
   __syncthreads();
   for (int k = 2; k <= p2; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < p2; i += kPlanThreads) {
+      for (int i = tid; i < p2; i += nthreads) {
         const int ixj = i ^ j;
         if (ixj > i) {
           const uint32_t a = keys[i], c = keys[ixj];
@@ -183,7 +189,7 @@ mla_plan_kernel(int B, int H, int max_q, int W, int items_cap, int p2cap,
       __syncthreads();
     }
   }
-  for (int k = tid; k < items_cap; k += kPlanThreads) {
+  for (int k = tid; k < items_cap; k += nthreads) {
     int32_t* rec = plan + off_i + 4LL * k;
     if (k < n_items) {
       const int e = (int)(keys[k] & 0xFFFFu);
@@ -222,10 +228,15 @@ mla_status launch_plan_device(const mla_plan_params& p, const int32_t* kv_indptr
       return MLA_ERR_CUDA;
     attr_set[dev] = smem;
   }
-  mla_plan_kernel<<<1, kPlanThreads, smem, (cudaStream_t)stream>>>(
-      p.batch, p.num_heads, p.max_q_len, p.num_workers, g.items_cap, p2cap, kv_indptr, qo_indptr,
-      plan, ws_hdr);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  // threads: the larger of the batch and the item capacity, rounded up to a
+  // power of two in [64, 1024]
+  int threads = 64;
+  while (threads < kPlanThreadsMax && (threads < p.batch + 1 || threads < g.items_cap)) threads <<= 1;
+  return launch_overlapped(mla_plan_kernel, dim3(1), dim3(threads), smem, (cudaStream_t)stream, p.batch,
+                           p.num_heads, p.max_q_len, p.num_workers, g.items_cap, p2cap, kv_indptr, qo_indptr,
+                           plan, ws_hdr) == cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
 }
 
 }  // namespace mla
