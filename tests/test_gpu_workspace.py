@@ -69,3 +69,32 @@ def test_reading_a_fault_clears_the_state():
     O2, L2, _ = hz.run(w, algo=m.MLA_ALGO_TENSOR, runner=runner, dev=dev)
     Oref, Lref = mo.mla_decode_workload(w)
     hz.assert_close(O2, L2, Oref, Lref, w.kv_dtype, what=w.name)
+
+
+@pytest.mark.parametrize("algo", [m.MLA_ALGO_CUDA_CORE, m.MLA_ALGO_TENSOR], ids=["cuda_core", "tensor"])
+def test_back_to_back_calls_with_changing_lengths(algo):
+    """Six DYNAMIC calls queued on one stream with no synchronisation between them,
+    on one plan buffer and workspace, each with other lengths, T and indices: the
+    planner of a call may start while the previous call's decode still runs (an
+    overlapped launch) and must not rewrite the plan before that decode is done.
+    Every call's output matches the oracle."""
+    slots = mi.long_skewed_pool_slots(3, scale=1 / 64)
+    ws = [mi.long_skewed_fp8(replay=r, scale=1 / 64, num_slots=slots) for r in range(3)]
+    devs = [mi.to_device(w) for w in ws]
+    maxq = max(int(w.q_lens().max()) for w in ws)
+    runner = m.DecodeRunner(ws[0].batch, ws[0].num_heads, maxq, mode=m.MLA_PLAN_DYNAMIC, num_workers=76)
+    outs = []
+    for k in range(6):
+        w, dev = ws[k % 3], devs[k % 3]
+        o = torch.full((w.total_q, w.num_heads, 512), float("nan"), device="cuda", dtype=torch.bfloat16)
+        lse = torch.full((w.total_q, w.num_heads), float("nan"), device="cuda", dtype=torch.float32)
+        runner.forward(o=o, lse=lse, algo=algo, **dev)
+        outs.append((k % 3, o, lse))
+    torch.cuda.synchronize()
+    assert hz.device_error(runner) == (0, 0)
+    refs = [mo.mla_decode_workload(w) for w in ws]
+    for r, o, lse in outs:
+        hz.assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), *refs[r], "fp8",
+                        what=f"call of draw {r}")
+    queue, counters, _ = _state(runner)
+    assert not queue.any() and not counters.any()
