@@ -257,3 +257,36 @@ def test_wrong_mask_fails_tolerance(algo):
     Oref, Lref = mo.mla_decode_workload(w, requests=[0, 1])
     with pytest.raises(AssertionError):
         hz.assert_close(O, L, Oref, Lref, "fp8", rows=hz.rows_of(w, [0, 1]))
+
+
+@pytest.mark.parametrize("heads,t", [(127, 1), (128, 1), (129, 1), (85, 3), (128, 2), (257, 1)],
+                         ids=["rows127", "rows128", "rows129", "rows255", "rows256", "rows257"])
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_row_counts_around_the_item_halves(algo, heads, t, kv_dtype):
+    """Query rows per request just below, at and above a CTA's 128 rows and an item's
+    256 (the second CTA of a pair empty, one row, full; a second item of one row),
+    with KV long enough for the planner to give every row group 16 splits."""
+    w = mi.make_workload(f"halves_{heads}x{t}", batch=2, num_heads=heads, q_lens=[t, t],
+                         kv_lens=[16 * 128 * 4 + 77, 300], kv_dtype=kv_dtype, causal=True,
+                         seed=53 + heads + t, num_slots=16384)
+    runner_w = 4096
+    O, L, runner = hz.run(w, algo=algo, num_workers=runner_w)
+    assert hz.device_error(runner) == (0, 0)
+    # the long request's row groups use the largest split count
+    assert int(runner.plan_d[16]) == 16
+    Oref, Lref = mo.mla_decode_workload(w)
+    hz.assert_close(O, L, Oref, Lref, kv_dtype, what=w.name)
+
+
+def test_empty_batch_is_a_no_op(algo):
+    runner = m.DecodeRunner(0, 16, 1, mode=m.MLA_PLAN_DYNAMIC, num_workers=8)
+    z32 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q = torch.zeros(1, 16, 576, dtype=torch.bfloat16, device="cuda")
+    pool = torch.zeros(4, 576, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros(1, 16, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 16, dtype=torch.float32, device="cuda")
+    runner.forward(q=q, kv_pool=pool, kv_dtype=m.MLA_KV_BF16, kv_indptr=z32, kv_indices=z32,
+                   qo_indptr=z32, causal=True, softmax_scale=0.07, kv_scale=1.0, o=o, lse=lse, algo=algo)
+    torch.cuda.synchronize()
+    assert hz.device_error(runner) == (0, 0)
+    assert not o.any() and not lse.any()
