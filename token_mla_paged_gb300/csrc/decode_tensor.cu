@@ -147,6 +147,8 @@ __device__ __forceinline__ uint32_t swz(int r, int u) { return (uint32_t)(r * 12
 // Epilogue staging, 64-byte rows: unit u of row r (bank-conflict free for 8 rows).
 __device__ __forceinline__ uint32_t swz64(int r, int u) { return (uint32_t)(r * 64 + ((u ^ ((r >> 1) & 3)) << 4)); }
 
+constexpr long long kAbortDrainCycles = 200000;   // ~100 µs at GB300 clocks
+
 // On a failed wait: record, raise the abort flag in all four CTAs.
 __device__ __noinline__ void fail(Bars* bars, const DecodeParams& p, int site) {
   record_error(p.ws_hdr, MLA_DEV_WAIT_TIMEOUT, site);
@@ -1014,6 +1016,15 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
   }
 
 done:
+  // A CTA that gave up on a wait lets what was issued before the abort (its own
+  // gathers and MMAs, the P copies it sent into a peer) land before the cluster
+  // releases its memory: a fixed ~100 µs, far longer than any copy or MMA takes.
+  // A completed call never takes this branch.
+  if (*reinterpret_cast<volatile int*>(&bars->abort)) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < kAbortDrainCycles) {
+    }
+  }
   fence_before_sync();
   __syncthreads();
   cluster_sync();        // the pairs' MMAs and every remote arrival are finished
