@@ -84,6 +84,11 @@ constexpr int kPChunk = kHalfRows * 128;       // P: [128 rows][64 entries bf16]
 constexpr int kPBytes = 2 * kPChunk;           // 128 entries
 constexpr int kPStatsOff = kPBytes;            // alpha[128], m[128], l[2][128] (per column half), flags[4]
 constexpr int kPCopyBytes = kPBytes + 4 * 512 + 64;  // bytes handed over per tile, a multiple of 16
+// Q of an item on the score side: 128 rows x 576 bf16 = nine 16 KB chunks of 64
+// columns (128-byte swizzled, like K), staged in the two KV stages.
+constexpr int kQChunk = kHalfRows * 128;
+constexpr int kQIssuers = 7;                   // warps 9-15 gather Q (bf16: all gather warps; fp8: with the converters)
+constexpr int kQBytes = 9 * kQChunk;
 constexpr int kPBufBytes = 35 * 1024;          // buffer stride: each P buffer starts on a swizzle atom
 
 // Shared-memory map (identical offsets in all four CTAs; barriers first).
@@ -99,6 +104,7 @@ constexpr int kOffEpi0 = kOffTiles + kOStageUsed;
 constexpr int kOffEpi1 = kOffTiles + kStageBytes + kOStageUsed;
 static_assert(kStageBytes - kOStageUsed == 8192, "epilogue staging");
 static_assert(kSmemBytes + kSmemAlign <= 232448, "shared memory");
+static_assert(kQBytes == kStages * kStageBytes && kQChunk % 1024 == 0, "Q staging fills the two KV stages");
 // Every operand the MMA reads through a 128-byte-swizzle descriptor starts on a
 // 1024-byte boundary (the swizzle is a function of the address bits).
 static_assert(kOffTiles % 1024 == 0 && kStageBytes % 1024 == 0 && kOffPBuf % 1024 == 0 &&
@@ -127,6 +133,8 @@ struct Bars {
   uint64_t corr[kPBufs];      // output, even rank: both CTAs hold P and have rescaled O
   uint64_t o_ready[kPBufs];   // output: PV with this P buffer done
   uint64_t o_free;            // output, even rank: both epilogues read O
+  uint64_t q_land;            // score: the item's Q rows landed in the (free) KV stages
+  uint64_t q_copied;          // score: the row warps moved them into TMEM
   uint64_t mrg_b;             // output: warp 0 published the split's verdict (partial / merge)
   uint64_t mrg_c;             // output: the row warps fenced their partial rows
   uint64_t never;             // failure-path test: nothing ever arrives here
@@ -273,10 +281,35 @@ __device__ __forceinline__ void stage_and_write(const float (&v)[32], bool f32, 
   }
 }
 
+// Score side, at the start of an item: once the previous item's QK^T is done with
+// both KV stages (their `empty` phases for tiles kseq-1 and kseq-2), gather the
+// item's live Q rows of this CTA's half into them: 9 chunks of 64 columns, groups of
+// 4 rows, one gather4 per lane over `nissue` warps (this one is number `wi`).  The
+// last group repeats the half's last live row.  Rows that are not live are not
+// loaded: their Q only feeds their own, masked, S rows.  (The caller waits for the
+// stages to be free.)
+__device__ __forceinline__ uint32_t q_groups(const Item& it, int half) {
+  const int hrows = min(max(it.nrows - kHalfRows * half, 0), kHalfRows);
+  return (uint32_t)((hrows + 3) / 4);
+}
+__device__ __forceinline__ void stage_q(const Item& it, int half, uint32_t tiles_u32, const CUtensorMap* tmap_q,
+                                        uint64_t* q_land, int wi, int nissue, int lane) {
+  const int ng = (int)q_groups(it, half);
+  const int64_t row0 = it.q_row_base + it.row0 + kHalfRows * half;
+  const int last = min(it.nrows - kHalfRows * half, kHalfRows) - 1;
+  for (int o = wi * 32 + lane; o < 9 * ng; o += nissue * 32) {
+    const int c = o / ng, g = o - c * ng;
+    const int r0 = 4 * g;
+    tma_gather4(tiles_u32 + (uint32_t)(c * kQChunk + g * 512), tmap_q, 64 * c, (int32_t)(row0 + min(r0, last)),
+                (int32_t)(row0 + min(r0 + 1, last)), (int32_t)(row0 + min(r0 + 2, last)),
+                (int32_t)(row0 + min(r0 + 3, last)), q_land);
+  }
+}
+
 template <bool kFp8>
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, 1)
 mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                         const DecodeParams p) {
+                         const __grid_constant__ CUtensorMap tmap_q, const DecodeParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((kSmemAlign - (smem_u32(smem_raw) & (kSmemAlign - 1))) & (kSmemAlign - 1));
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
@@ -312,6 +345,8 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       mbar_init(&bars->o_ready[b], 1);
     }
     mbar_init(&bars->o_free, 2 * kRowWarps);
+    mbar_init(&bars->q_land, 1);
+    mbar_init(&bars->q_copied, kRowWarps);
     mbar_init(&bars->mrg_b, 1);
     mbar_init(&bars->mrg_c, kRowWarps);
     mbar_init(&bars->never, 1);
@@ -325,6 +360,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
   if (warp == kWarpAux0 && lane == 0) {
     prefetch_tmap(&tmap_k);
     prefetch_tmap(&tmap_v);
+    prefetch_tmap(&tmap_q);
   }
   fence_before_sync();
   __syncthreads();
@@ -370,7 +406,7 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
     const int e_sub = score_cta ? kHalfN * half : 0;          // first tile entry this CTA gathers
     const int nidx = ngroups / 8;                             // index registers in use (2 | 4)
     const void* tmap = score_cta ? (const void*)&tmap_k : (const void*)&tmap_v;
-    uint32_t kseq = 0;
+    uint32_t kseq = 0, qseq = 0;
     const bool report = pw == 0;
     // Raw slot indices of tile j: lane holds entries lane + 32k (k < nidx), -1 past
     // the end; checked only when used, one iteration later, so the load is not waited on.
@@ -393,6 +429,21 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       const int nt = item_tiles(it);
       int32_t nx[4] = {-1, -1, -1, -1};
       if (nt > 0) tile_idx(it, 0, nx);
+      if (score_cta && nt > 0) {
+        // The item's Q rows pass through the KV stages (the fp8 conversion warps issue
+        // their share too), then the stages go back to the KV tiles.
+        for (int k = 1; k <= kStages; ++k)
+          if ((int)kseq - k >= 0) {
+            const uint32_t s = kseq - k;
+            WAITC(&bars->empty[s % kStages], (s / kStages) & 1, 8);
+          }
+        if (pw == 0 && lane == 0) mbar_arrive_expect_tx(&bars->q_land, 9 * 512 * q_groups(it, half));
+        __syncwarp();
+        stage_q(it, half, smem_u32(tiles), &tmap_q, &bars->q_land, pw, kQIssuers, lane);
+        __syncwarp();
+        WAITC(&bars->q_copied, qseq & 1, 9);
+        ++qseq;
+      }
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         const uint32_t ph = (kseq / kStages) & 1;
@@ -462,6 +513,16 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
     FOR_ITEMS(idx) {
       const Item it = load_item(p, idx);
       const int nt = item_tiles(it);
+      if (score_cta && nt > 0) {
+        // this warp's share of the item's Q gathers, once both stages are free
+        for (int k = 1; k <= kStages; ++k)
+          if ((int)kseq - k >= 0) {
+            const uint32_t s = kseq - k;
+            WAITC(&bars->empty[s % kStages], (s / kStages) & 1, 7);
+          }
+        stage_q(it, half, smem_u32(tiles), &tmap_q, &bars->q_land, 3 + cw, kQIssuers, lane);
+        __syncwarp();
+      }
       for (int j = 0; j < nt; ++j, ++kseq) {
         const int st = kseq % kStages;
         WAIT(&bars->full8[st], (kseq / kStages) & 1, 4);
@@ -636,22 +697,23 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       // column); column half 0 loads units [0, 40), half 1 units [40, 72).
       WAITC(&bars->q_free, (qitem & 1) ^ 1, 30);
       if (warp == 0 && lane == 0) prefetch_q_rows(p, item_of(r_ + 1, cluster, n_clusters), n_items, half);
-      fence_after_sync();
+      // Q rows of this half -> TMEM (A operand layout: lane = row, two bf16 per
+      // column), from the staging the gather warps filled: column half 0 moves chunks
+      // [0, 5), half 1 chunks [5, 9).
+      WAIT(&bars->q_land, qitem & 1, 35);
       {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                          (it.q_row_base + hrow0 + (live ? r : 0)) * kDqk);
-        const int c_beg = ch ? 5 : 0, c_end = ch ? 9 : 5;   // TMEM chunks of 32 columns (8 units)
+        const int rr = 32 * q4 + lane;
+        const int c_beg = ch ? 5 : 0, c_end = ch ? 9 : 5;   // 64-column chunks = 32 TMEM columns
         for (int c0 = c_beg; c0 < c_end; ++c0) {
-          uint4 u[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) u[k] = live ? __ldg(src + c0 * 8 + k) : make_uint4(0, 0, 0, 0);
+          const uint8_t* chunk = tiles + c0 * kQChunk;
           uint32_t v[32];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            v[4 * k] = u[k].x;
-            v[4 * k + 1] = u[k].y;
-            v[4 * k + 2] = u[k].z;
-            v[4 * k + 3] = u[k].w;
+            const uint4 u = *reinterpret_cast<const uint4*>(chunk + swz(rr, k));
+            v[4 * k] = u.x;
+            v[4 * k + 1] = u.y;
+            v[4 * k + 2] = u.z;
+            v[4 * k + 3] = u.w;
           }
           tmem_st32(tmem + lane_addr + kTmemQ + 32 * c0, v);
         }
@@ -659,7 +721,10 @@ mla_decode_tensor_kernel(const __grid_constant__ CUtensorMap tmap_k, const __gri
       }
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) arrive_at(&bars->q_full, lead, rank);
+      if (lane == 0) {
+        mbar_arrive(&bars->q_copied);                    // the stages go back to the KV gathers
+        arrive_at(&bars->q_full, lead, rank);
+      }
       ++qitem;
 
       // Visibility: local entry i is visible to this row iff ibeg <= i < iend, its
@@ -1063,6 +1128,20 @@ bool encode_pool_map(EncodeTiledFn enc, CUtensorMap* tm, const DecodeParams& dp,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row-gather tensor map over q [rows, 576] bf16, one row high and 64 columns wide
+// (128-byte swizzled).  The row extent is an upper bound of the call's query rows
+// (batch x max_q_len x heads): the kernel asks only for rows of its own items.
+bool encode_q_map(EncodeTiledFn enc, CUtensorMap* tm, const DecodeParams& dp) {
+  const int64_t rows = (int64_t)dp.batch * dp.max_q_len * dp.num_heads;
+  const cuuint64_t gdim[2] = {(cuuint64_t)kDqk, (cuuint64_t)(rows > 0 ? rows : 1)};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kDqk * 2};
+  const cuuint32_t boxd[2] = {64u, 1u};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(dp.q), gdim, gstride, boxd, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of this kernel that fit on the device at once (cached per device).
 template <bool kFp8>
 int max_active_clusters(int dev) {
@@ -1094,9 +1173,10 @@ template <bool kFp8>
 mla_status launch_impl(const DecodeParams& dp, void* stream) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return MLA_ERR_CUDA;
-  CUtensorMap tk, tv;
+  CUtensorMap tk, tv, tq;
   if (!encode_pool_map(enc, &tk, dp, kFp8, kFp8 ? 192u : 64u)) return MLA_ERR_INVALID_ARG;
   if (!encode_pool_map(enc, &tv, dp, kFp8, kFp8 ? 128u : 64u)) return MLA_ERR_INVALID_ARG;
+  if (!encode_q_map(enc, &tq, dp)) return MLA_ERR_INVALID_ARG;
   int clusters = max_active_clusters<kFp8>(current_device_slot());
   if (clusters < 1) return MLA_ERR_CUDA;
   if (clusters > dp.items_cap) clusters = dp.items_cap > 0 ? dp.items_cap : 1;
@@ -1107,7 +1187,7 @@ mla_status launch_impl(const DecodeParams& dp, void* stream) {
     kp.out_scale = dp.out_scale * 5.192296858534828e33f;
   }
   return launch_overlapped(mla_decode_tensor_kernel<kFp8>, dim3(4 * clusters), dim3(kThreads),
-                           kSmemBytes + kSmemAlign, (cudaStream_t)stream, tk, tv, kp) == cudaSuccess
+                           kSmemBytes + kSmemAlign, (cudaStream_t)stream, tk, tv, tq, kp) == cudaSuccess
              ? MLA_OK
              : MLA_ERR_CUDA;
 }
