@@ -100,14 +100,24 @@ def algorithmic_bytes(w) -> int:
     return nnz * 576 * elem + 4 * nnz + pos_bytes + rows * (576 * 2 + 512 * 2 + 4)
 
 
+def kernel_code_hash(path: str) -> str:
+    """sha256 prefix of a CUDA source's code: line comments, trailing blanks and
+    empty lines dropped, so editing a comment does not count as changing the kernel."""
+    import hashlib
+    lines = []
+    for line in open(path, encoding="utf-8").read().splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def ncu_traffic(config: str, record: str = "ncu_traffic.json"):
     """DRAM bytes of one launch from a committed ncu capture, only if the kernel
-    source is the one that was profiled; else None."""
-    import hashlib
+    code is the one that was profiled; else None."""
     try:
         d = json.load(open(os.path.join(ROOT, "profiles", record)))
-        src = open(os.path.join(ROOT, d["kernel_source"]), "rb").read()
-        if hashlib.sha256(src).hexdigest()[:16] != d["kernel_source_sha256_16"]:
+        if kernel_code_hash(os.path.join(ROOT, d["kernel_source"])) != d["kernel_code_sha256_16"]:
             return None
         return d["workloads"].get(config, {}).get("dram_bytes")
     except Exception:

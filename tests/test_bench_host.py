@@ -72,18 +72,21 @@ def test_algorithmic_bytes_from_shapes():
     assert bench.absorb_bytes(256, 128, 128, 512) == bench.absorb_bytes(256, 128, 512, 128) == 50331648
 
 
-def test_ncu_traffic_only_for_the_profiled_source(tmp_path, monkeypatch):
+def test_ncu_traffic_only_for_the_profiled_code(tmp_path, monkeypatch):
     src = tmp_path / "kernel.cu"
-    src.write_text("// profiled version\n")
+    src.write_text("// profiled version\nint a = 1;  // one\n")
     (tmp_path / "profiles").mkdir()
-    rec = {"kernel_source": "kernel.cu",
-           "kernel_source_sha256_16": hashlib.sha256(src.read_bytes()).hexdigest()[:16],
+    code = hashlib.sha256("int a = 1;".encode()).hexdigest()[:16]
+    assert bench.kernel_code_hash(str(src)) == code
+    rec = {"kernel_source": "kernel.cu", "kernel_code_sha256_16": code,
            "workloads": {"w": {"dram_bytes": 1234}}}
     (tmp_path / "profiles" / "rec.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.ncu_traffic("w", "rec.json") == 1234
     assert bench.ncu_traffic("other", "rec.json") is None
-    src.write_text("// changed since\n")
+    src.write_text("// a comment edited\n\nint a = 1;   // still one\n")
+    assert bench.ncu_traffic("w", "rec.json") == 1234        # comments do not change the kernel
+    src.write_text("int a = 2;\n")
     assert bench.ncu_traffic("w", "rec.json") is None
 
 
@@ -92,4 +95,6 @@ def test_committed_records_name_existing_sources():
         if name.endswith(".json"):
             d = json.load(open(os.path.join(bench.ROOT, "profiles", name)))
             assert os.path.exists(os.path.join(bench.ROOT, d["kernel_source"])), name
-            assert len(d["kernel_source_sha256_16"]) == 16 and d["workloads"], name
+            assert len(d["kernel_code_sha256_16"]) == 16 and d["workloads"], name
+            # the committed kernel is the profiled one
+            assert bench.kernel_code_hash(os.path.join(bench.ROOT, d["kernel_source"])) == d["kernel_code_sha256_16"], name

@@ -3,7 +3,7 @@
 The persistent kernel re-plans the split from the real per-row KV lengths at every
 call, so a graph captured once stays correct while the KV grows ("[DSV4] Tuned ASM
 FP8 decode with split plans; HCA on aiter's persistent V4-NM kernel", Summary
-part 2).  The graph holds [memset, device planner, decode]; between replays the
+part 2).  The graph holds [device planner, decode]; between replays the
 index lists and query block are rewritten in place in buffers sized for capacity.
 """
 import numpy as np

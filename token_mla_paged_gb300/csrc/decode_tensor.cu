@@ -6,7 +6,9 @@
 // entries, and runs on a cluster of four CTAs on four SMs:
 //
 //   ranks 0 and 1, the score pair: rank h holds query rows [128h, 128h+128) of
-//     the item in TMEM (the A operand).  Each 128-entry KV tile is gathered
+//     the item in TMEM (the A operand), gathered by TMA into the two KV stages
+//     (exactly the 144 KB they hold) while they are free between items and moved
+//     into TMEM by the row warps.  Each 128-entry KV tile is gathered
 //     once per pair: rank h gathers entries [64h, 64h+64) of the tile, all 576
 //     columns.  One cta_group::2 MMA per 16 columns (M = 256 rows, N = 128
 //     entries, each CTA supplying half of N) writes S = Q K^T of the CTA's own
