@@ -729,6 +729,17 @@ def _timing_events_n(torch, n):
 REPLAYS_LONG = 5     # distinct length / T / index draws cycled through the long-skewed replays
 
 
+def decode_workers(config: str, w, algo: int, dev_index: int, override: int = 0) -> int:
+    """The plan's worker count for a decode workload: the override, else the tuned
+    value, else the clusters (tensor) or SMs (CUDA cores) of the device."""
+    import token_mla_paged_gb300 as m
+    # The draft block has 16 row groups of 256 rows over 64 KV tiles; 32 workers (two
+    # splits each, one item per cluster) measured faster than 64 (two items a cluster).
+    tuned = {"draft_block_bf16": 32} if algo == m.MLA_ALGO_TENSOR else {}
+    return override or tuned.get(config) or m.default_workers_for(
+        algo, w.batch, w.num_heads, int(w.q_lens().max()), dev_index)
+
+
 def roofline_of(flops: float, nbytes: float, seconds: float, peaks: dict) -> dict:
     """The roof that binds: max(bytes / HBM peak, FLOPs / bf16 tensor peak).  The
     kernel is timed per launch (about a millisecond), so the burst tensor peak is
@@ -765,11 +776,7 @@ def decode_main(args, rank: int, world: int):
     w, extra = build_workload(args.config)
     shards = extra["shards"]
     algo = m.MLA_ALGO_TENSOR if args.algo == "tensor" else m.MLA_ALGO_CUDA_CORE
-    # The draft block has 16 row groups of 256 rows over 64 KV tiles; 32 workers (two
-    # splits each, one item per cluster) measured faster than 64 (two items a cluster).
-    tuned = {"draft_block_bf16": 32} if algo == m.MLA_ALGO_TENSOR else {}
-    workers = args.workers or tuned.get(args.config) or m.default_workers_for(
-        algo, w.batch, w.num_heads, int(w.q_lens().max()), dev_index)
+    workers = decode_workers(args.config, w, algo, dev_index, args.workers)
     # Long skewed contexts: every replay brings new lengths, T and indices (the
     # persistent kernel re-plans from them); the other workloads replay one batch.
     replays = [w]
