@@ -88,3 +88,16 @@ def test_rope_rejects_bad_arguments():
     x = torch.zeros(4, 2, 512, dtype=torch.float32, device="cuda")
     with pytest.raises(m.MlaError):
         m.mla_rope_q_cache(x, x, x, x, x, None, None, None, None, m.MLA_KV_BF16)
+
+
+@pytest.mark.parametrize("style", [m.MLA_ROPE_NEOX, m.MLA_ROPE_INTERLEAVED], ids=["neox", "interleaved"])
+def test_rope_q_cache_full_size(style):
+    """The benchmarked size: 512 tokens x 128 heads into a 131072-slot fp8 pool with a
+    131072-position table; every q row and every pool row bit-exact."""
+    import bench
+    inp = mi.rope_inputs(bench.RC_TOKENS, bench.RC_HEADS, max_pos=bench.RC_MAXPOS, num_slots=bench.RC_SLOTS)
+    q, pool, pool0 = _run(inp, "fp8", style)
+    q_ref, pool_ref = rc.rope_q_cache(inp.q_nope_bits, inp.q_pe_bits, inp.kv_c_bits, inp.k_pe_bits, inp.positions,
+                                      inp.cos_sin, style, inp.slot_mapping, pool0, "fp8", 0.05)
+    assert np.array_equal(q, q_ref)
+    assert np.array_equal(pool, pool_ref)
